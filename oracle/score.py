@@ -1,0 +1,102 @@
+"""fp64 oracle of look-ahead attention scoring and max/max/mean aggregation.
+
+TEST INFRASTRUCTURE (see the package docstring for who may call it).
+
+Definitions followed:
+  * attention score a_ij = softmax(Q_{M+j} K^T / sqrt(d))_i for prompt token i
+    and look-ahead step j, per layer and query head -- paper review "Speculative
+    Prefill ...", section "core algorithm: token importance speculation" and the
+    first formula of section "core formulas";
+  * aggregation: max over heads, then max over layers, then mean over the N
+    look-ahead steps -- paper review, section "aggregate attention scores as
+    token importance" (max-mean aggregation over the [N, L, S, H] tensor), and
+    the llama.cpp guide "SpecPrefill -- Implementation Guide", section "Token
+    Importance" and its function compute_imp.
+
+Inputs are numpy arrays of real values (fp32 or fp64) or uint16 arrays, which
+are read as bf16 bit patterns (value = the bits shifted into the high half of
+an fp32).  All arithmetic is fp64.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype == np.uint16:                        # bf16 bit patterns
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def lookahead_rows(Q_la, K_la, l: int, h: int, G: int) -> np.ndarray:
+    """Causal look-ahead logits u[j, k] = Q_la[j,l,h] . K_la[l,g,k] / sqrt(d), k <= j.
+
+    Entries with k > j are -inf (look-ahead step j has not seen later steps).
+    """
+    N, d = Q_la.shape[0], Q_la.shape[3]
+    g = h // G
+    q = _f64(Q_la[:, l, h, :])                      # [N, d]
+    kla = _f64(K_la[l, g])                          # [N, d]
+    u = (q @ kla.T) / math.sqrt(d)                  # [N, N]
+    u[np.triu_indices(N, k=1)] = -np.inf
+    return u
+
+
+def _softmax_rows(s: np.ndarray, u: np.ndarray):
+    """Row-wise softmax over [prompt logits s[j] | look-ahead logits u[j, :j+1]]."""
+    N = s.shape[0]
+    a = np.empty_like(s)
+    a_la = np.zeros_like(u)
+    for j in range(N):
+        row = np.concatenate([s[j], u[j, :j + 1]])
+        m = row.max()
+        lse = m + math.log(np.exp(row - m).sum())
+        a[j] = np.exp(s[j] - lse)
+        a_la[j, :j + 1] = np.exp(u[j, :j + 1] - lse)
+    return a, a_la
+
+
+def attention_rows(Q_la, K_prompt, K_la, l: int, h: int, k64=None):
+    """Post-softmax attention of every look-ahead query of (layer l, head h).
+
+    Returns (a[N, M], a_la[N, N]): a[j, i] is the weight of prompt token i and
+    a_la[j, k] that of look-ahead key k (zero for k > j).  Every row of
+    [a | a_la] sums to 1.  ``k64`` may pass K_prompt[l, g] already in fp64.
+    """
+    N, L, H, d = Q_la.shape
+    H_kv = K_prompt.shape[1]
+    G = H // H_kv
+    g = h // G
+    q = _f64(Q_la[:, l, h, :])                      # [N, d]
+    k = _f64(K_prompt[l, g]) if k64 is None else k64   # [M, d]
+    s = (q @ k.T) / math.sqrt(d)                    # [N, M] prompt logits
+    u = lookahead_rows(Q_la, K_la, l, h, G)         # [N, N] look-ahead logits
+    return _softmax_rows(s, u)
+
+
+def importance(Q_la, K_prompt, K_la) -> np.ndarray:
+    """importance_i = (1/N) sum_j max_{l,h} a[l,h,j,i]   (fp64, shape [M]).
+
+    Q_la[N, L, H, d], K_prompt[L, H_kv, M, d], K_la[L, H_kv, N, d].  With N = 0
+    every token gets importance 1.0 (compute_imp's fallback when no step was
+    captured).
+    """
+    N, L, H, d = Q_la.shape
+    H_kv, M = K_prompt.shape[1], K_prompt.shape[2]
+    G = H // H_kv
+    if N == 0:
+        return np.ones(M, dtype=np.float64)
+    best = np.zeros((N, M), dtype=np.float64)       # max over (l, h) so far; weights are >= 0
+    for l in range(L):
+        for g in range(H_kv):
+            k64 = _f64(K_prompt[l, g])
+            for h in range(g * G, (g + 1) * G):
+                a, _ = attention_rows(Q_la, K_prompt, K_la, l, h, k64=k64)
+                np.maximum(best, a, out=best)
+    total = np.zeros(M, dtype=np.float64)
+    for j in range(N):                              # mean over look-ahead steps, j in order
+        total += best[j]
+    return total / N
