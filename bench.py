@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Throughput of SpecPrefill token-importance scoring + chunk selection on GB300.
+
+One step = sp_score (look-ahead attention importance over the whole K cache)
+followed by sp_select (chunk mean -> avg pool -> top-K -> position IDs) on one
+synthetic prompt of the Llama-3.1-8B-shaped speculator at M = 32768 tokens
+(L=32, H=32, H_kv=8, d=128, N=8, bf16, chunk 32, pool 3, keep 10%).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--config I]
+
+Prints one JSON line (rank 0).  value = prompt tokens scored+selected per second
+over all ranks (each rank runs its own replica: weak scaling), timed with CUDA
+events on the launching stream, inputs resident in HBM; the K cache (2 GiB) is
+far larger than L2 and L2 is also flushed between timed steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prompt tokens scored+selected/sec at M=32K; K-cache HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", type=int, default=2, help="workload index (default 2: 8B shape, M=32K)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 8:
+                    continue
+                try:
+                    rows.append((float(p[0]), float(p[1]), p[3:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, r in rows:
+            for n, v in zip(names, r[1:5]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# measured peaks, ncu traffic record
+# ----------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_prefill_token_sp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("score") or name.endswith(".cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(config_name: str):
+    """DRAM bytes per sp_score call from the committed ncu summary, if it was
+    taken on the current scoring sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(config_name)
+    if not ent or ent.get("scoring_sources_sha256") != kernel_source_digest():
+        return None
+    return ent.get("dram_bytes_per_call")
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timings (test infrastructure, the only place bench runs it)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(x, layers: int):
+    """Time the fp64 oracle on the first `layers` layers plus the full selection;
+    returns (seconds for the scoring sample, seconds for the selection)."""
+    import numpy as np
+    import oracle
+    wl = x.wl
+    t0 = time.perf_counter()
+    imp = oracle.importance(x.Q_la[:, :layers], x.K_prompt[:layers], x.K_la[:layers])
+    t1 = time.perf_counter()
+    oracle.select(imp.astype(np.float32), wl.chunk, wl.pool_k, wl.mode, wl.keep_rate or wl.mass, wl.boost)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(x, budget_s: float = 12.0):
+    wl = x.wl
+    layers, spent = 0, 0.0
+    t_layers, t_sel = 0.0, 0.0
+    while layers < wl.L and spent < budget_s:
+        n = 1 if layers == 0 else min(wl.L - layers, max(1, int(layers * (budget_s - spent) / max(spent, 1e-9))))
+        n = min(n, wl.L - layers)
+        ts, tsel = oracle_sample(_slice_layers(x, layers, n), n)
+        t_layers += ts
+        t_sel = tsel
+        layers += n
+        spent += ts + tsel
+    est = t_layers / layers * wl.L + t_sel
+    return {"value": wl.M / est, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle on {layers} of {wl.L} layers of {wl.name} (+ full selection), "
+                      f"scaled to all layers: {est:.2f} s per prompt"}
+
+
+def _slice_layers(x, start, n):
+    import dataclasses
+    return dataclasses.replace(x, Q_la=x.Q_la[:, start:start + n], K_prompt=x.K_prompt[start:start + n],
+                               K_la=x.K_la[start:start + n])
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    wl = W.CONFIGS[args.config]
+    x = W.make_inputs(wl, args.config)
+    per_step = []
+    for k in range(args.warmup + args.steps):
+        ts, tsel = oracle_sample(x, 1)
+        if k >= args.warmup:
+            per_step.append(ts * wl.L + tsel)
+    ms = statistics.mean(per_step) * 1e3
+    value = wl.M / (ms / 1e3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "M": wl.M, "L": wl.L, "H": wl.H, "H_kv": wl.H_kv, "d": wl.d,
+                       "N": wl.N, "chunk": wl.chunk, "pool_k": wl.pool_k, "keep_rate": wl.keep_rate,
+                       "sample": "each step times 1 layer of scoring and the full selection, scaled to "
+                                 f"{wl.L} layers"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"1 of {wl.L} layers per step, scaled"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args) -> None:
+    import numpy as np
+    import torch
+
+    import speculative_prefill_token_sp_gb300 as sp
+    import workloads as W
+    from speculative_prefill_token_sp_gb300 import build as B
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    B.build()
+    dev = torch.device("cuda", local)
+    wl = W.CONFIGS[args.config]
+    assert wl.batch == 1, "bench runs a single-prompt workload"
+    x = W.make_inputs(wl, args.config)
+
+    def upload(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    Q, K, Kla = upload(x.Q_la), upload(x.K_prompt), upload(x.K_la)
+    dt = sp.SP_BF16 if wl.dtype == "bf16" else sp.SP_F32
+    M = wl.M
+    imp = torch.empty(M, dtype=torch.float32, device=dev)
+    kept = torch.empty(M, dtype=torch.int32, device=dev)
+    n_kept = torch.empty(1, dtype=torch.int64, device=dev)
+    ws_s_bytes = sp.sp_score_workspace_size(wl.L, wl.H, wl.H_kv, wl.d, M, wl.N, dt)
+    ws_k_bytes = sp.sp_select_workspace_size(M, wl.chunk)
+    ws_s = torch.empty(ws_s_bytes, dtype=torch.uint8, device=dev)
+    ws_k = torch.empty(ws_k_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rate = wl.keep_rate if wl.mode == "topk" else wl.mass
+    mode = sp.SP_SELECT_TOPK if wl.mode == "topk" else sp.SP_SELECT_MASS
+
+    def score_call():
+        s = sp.sp_score(Q, K, Kla, wl.L, wl.H, wl.H_kv, wl.d, M, wl.N, dt, imp, ws_s, ws_s_bytes, stream)
+        if s != sp.SP_OK:
+            raise sp.SpError(s, sp.sp_last_error())
+
+    def select_call():
+        s = sp.sp_select(imp, M, wl.chunk, wl.pool_k, mode, rate, wl.boost, kept, n_kept, ws_k, ws_k_bytes, stream)
+        if s != sp.SP_OK:
+            raise sp.SpError(s, sp.sp_last_error())
+
+    def step():
+        score_call()
+        select_call()
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = sp.sp_workspace_status(ws_s, stream)
+    if st != sp.SP_OK:
+        raise sp.SpError(st, sp.sp_last_error())
+
+    # -------- timed region: K steps, L2 flushed between steps --------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches0 = sp.sp_kernel_launches()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        # keep the GPU busy a little longer so the sampler sees the loaded clock
+        t_end = time.time() + 0.5
+        while time.time() < t_end:
+            step()
+            torch.cuda.synchronize()
+    launches = sp.sp_kernel_launches() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    value = world * M * args.steps / (total_ms / 1e3)
+    timed_launches = launches - 0  # includes the clock-tail steps; recount below
+    per_step_launches = None
+
+    # -------- dominant kernel(s): sp_score alone, per launch --------
+    n_roof = max(args.steps, 10)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_roof)]
+    l0 = sp.sp_kernel_launches()
+    for k in range(n_roof):
+        flush.zero_()
+        ev2[k][0].record(stream)
+        score_call()
+        ev2[k][1].record(stream)
+    torch.cuda.synchronize()
+    score_launches = (sp.sp_kernel_launches() - l0) // n_roof
+    l0 = sp.sp_kernel_launches()
+    step()
+    torch.cuda.synchronize()
+    per_step_launches = sp.sp_kernel_launches() - l0
+    score_ms = statistics.mean(a.elapsed_time(b) for a, b in ev2)
+    k_bytes = wl.k_bytes_per_token() * M
+    peak, peak_kind = hbm_peak()
+    achieved = k_bytes / (score_ms / 1e3) / 1e9
+
+    # -------- end to end through the public API, host buffers --------
+    hQ = torch.from_numpy(x.Q_la.view(np.int16) if x.Q_la.dtype == np.uint16 else x.Q_la).pin_memory()
+    hK = torch.from_numpy(x.K_prompt.view(np.int16) if x.K_prompt.dtype == np.uint16 else x.K_prompt).pin_memory()
+    hKla = torch.from_numpy(x.K_la.view(np.int16) if x.K_la.dtype == np.uint16 else x.K_la).pin_memory()
+    h_kept = torch.empty(M, dtype=torch.int32).pin_memory()
+    h_n = torch.empty(1, dtype=torch.int64).pin_memory()
+    Qv, Kv, Klav = (t.view(torch.int16) if t.dtype == torch.bfloat16 else t for t in (Q, K, Kla))
+    h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hKla))
+    d2h = h_kept.numel() * 4 + 8
+    n_e2e = max(3, min(args.steps, 10))
+    ev3 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+    for k in range(n_e2e):
+        ev3[k][0].record(stream)
+        Qv.copy_(hQ, non_blocking=True)
+        Kv.copy_(hK, non_blocking=True)
+        Klav.copy_(hKla, non_blocking=True)
+        step()
+        h_n.copy_(n_kept, non_blocking=True)
+        h_kept.copy_(kept, non_blocking=True)
+        ev3[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev3), world)
+    e2e_value = world * M / (e2e_ms / 1e3)
+
+    # sanity: the kept count follows the top-K rule
+    if wl.mode == "topk":
+        nc = (M + wl.chunk - 1) // wl.chunk
+        import math
+        kc = max(1, math.ceil(float(np.float32(nc) * np.float32(wl.keep_rate))))
+        assert int(h_n.item()) <= kc * wl.chunk
+
+    if rank != 0:
+        barrier(world)
+        return
+    clk = clocks.summary()
+    traffic = recorded_traffic(wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "M": M, "L": wl.L, "H": wl.H, "H_kv": wl.H_kv, "d": wl.d, "N": wl.N,
+                   "chunk": wl.chunk, "pool_k": wl.pool_k, "keep_rate": wl.keep_rate,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (K cache 2 GiB) and L2 flushed between timed steps"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "sp_score (all scoring kernels of one call)", "launch_ms": score_ms,
+                     "launches_per_call": score_launches, "algorithmic_bytes": k_bytes},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": per_step_launches * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x)
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+def main(argv=None) -> None:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_gpu(args)
+    _, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * specprefill.h -- C ABI of libspecprefill.so: SpecPrefill token-importance
+ * scoring and chunk selection on one NVIDIA GB300 (sm_103a).
+ *
+ * The method (paper review "Speculative Prefill: Turbocharging TTFT with
+ * Lightweight and Training-Free Token Importance Estimation", sections "core
+ * algorithm" and "core formulas"; llama.cpp guide "SpecPrefill --
+ * Implementation Guide", sections "How It Works", "v3 Improvements" and
+ * "v3.1 Optimizations"): a small speculator model has a post-RoPE key cache for
+ * an M-token prompt and the queries of N look-ahead decode steps.  Every
+ * prompt token i gets the importance
+ *
+ *     importance_i = (1/N) sum_j max_{l,h} softmax(Q_{M+j,l,h} K_{l,g(h)}^T / sqrt(d))_i
+ *
+ * where the softmax of look-ahead step j runs over the M prompt keys and the
+ * look-ahead keys 0..j.  The prompt is then cut into contiguous chunks, chunk
+ * scores are averaged (and pooled), chunks are selected, and the original
+ * position IDs of the kept tokens are returned in ascending order.  Decoding
+ * continues at positions M, M+1, ... (paper review, "position ID recovery").
+ *
+ * Conventions of every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, except
+ *    arguments whose name ends in "_host".  Layouts are row-major, last index
+ *    contiguous.  Data pointers must be 16-byte aligned.
+ *  - The library never allocates, frees or synchronises (except
+ *    sp_workspace_status).  Work is enqueued on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and runs asynchronously; outputs are
+ *    valid once the stream reaches that point.
+ *  - `ws` is a caller-owned device workspace of at least the size the matching
+ *    *_workspace_size function returns; its contents need not be initialised
+ *    and are overwritten.  One workspace must not be used by two calls that
+ *    may run at the same time.
+ *  - Errors: arguments are validated before anything is enqueued; on failure
+ *    the call returns a non-zero sp_status, enqueues nothing and
+ *    sp_last_error() describes the problem.  CUDA launch failures return
+ *    SP_ECUDA.  A kernel that detects a problem at run time (a bounded wait
+ *    that gave up) records it in the workspace; sp_workspace_status() reads it.
+ *    Nothing aborts the process.
+ */
+#ifndef SPECPREFILL_H
+#define SPECPREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SP_OK = 0,
+    SP_EINVAL = 1,        /* bad argument (shape, pointer, parameter range)          */
+    SP_ENOMEM = 2,        /* workspace smaller than *_workspace_size() asks for      */
+    SP_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed             */
+    SP_EDEVICE = 4,       /* a kernel recorded an internal error in the workspace    */
+    SP_ETIMEOUT = 5,      /* a bounded device-side wait gave up                      */
+    SP_EUNSUPPORTED = 6   /* valid, but outside what this build implements          */
+} sp_status;
+
+typedef enum { SP_BF16 = 0, SP_F32 = 1 } sp_dtype;
+
+typedef enum {
+    SP_SELECT_TOPK = 0,   /* chunk mean -> 1D average pool -> exactly kc chunks      */
+    SP_SELECT_MASS = 1    /* v3: chunks by mean until the cumulative mass >= tau    */
+} sp_mode;
+
+/* v3 structural boost (llama.cpp guide, "v3 Improvements: Structural Token
+ * Boosting" and "v3.1: Score Normalization").  Token scores are first min-max
+ * normalised to [0,1] over the prompt if `normalize` != 0 (all 1.0 when every
+ * score is equal), then multiplied by first_mult at positions [0, first_n) and
+ * by last_mult at positions [M - last_n, M) (both when the ranges overlap).
+ * The guide's defaults are {64, 1.5, 128, 1.3, 1}. */
+typedef struct {
+    int32_t first_n;
+    double  first_mult;
+    int32_t last_n;
+    double  last_mult;
+    int32_t normalize;
+} sp_boost;
+
+/* ------------------------------------------------------------------------ */
+/* Scoring                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes sp_score needs for this shape (0 if the shape is invalid). */
+size_t sp_score_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype);
+
+/* Token importance of one prompt.
+ *
+ * Defines: a[l,h,j,i] = softmax over {prompt keys 0..M-1, look-ahead keys
+ * 0..j} of Q_la[j,l,h,:] . key / sqrt(d), evaluated at prompt key i;
+ * importance[i] = (1/N) sum_j max_{l,h} a[l,h,j,i]   (paper review, "core
+ * formulas": attention score and importance aggregation; llama.cpp guide,
+ * "Token Importance": max over heads, max over layers, mean over look-ahead
+ * steps).  Query head h reads KV head h / (H / H_kv).
+ *
+ *   Q_la      [N, L, H, d]      look-ahead queries (post-RoPE), dtype
+ *   K_prompt  [L, H_kv, M, d]   prompt keys (post-RoPE), dtype
+ *   K_la      [L, H_kv, N, d]   look-ahead keys (post-RoPE), dtype
+ *   importance[M]               fp32 output
+ *   dtype     SP_BF16 or SP_F32 (all three inputs)
+ *
+ * Requirements: L, H, H_kv >= 1, H % H_kv == 0, 1 <= d <= 256, d % 8 == 0,
+ * M >= 0, 0 <= N, N * (H / H_kv) <= 256.  N == 0 writes importance 1.0 to
+ * every token (the guide's fallback when no look-ahead step was captured).
+ * M == 0 is a no-op.  Accuracy: importance within 1e-3 absolute and 1e-2
+ * relative of an fp64 evaluation on the same bf16 inputs; 1e-5 for fp32. */
+sp_status sp_score(const void* Q_la, const void* K_prompt, const void* K_la,
+                   int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype,
+                   float* importance, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for sp_score_varlen (cu_M_host: B+1 host prefix sums). */
+size_t sp_score_varlen_workspace_size(int B, const int64_t* cu_M_host, int L, int H, int H_kv,
+                                      int d, int N, sp_dtype dtype);
+
+/* Token importance of B independent prompts in one call.  Prompt b has
+ * M_b = cu_M_host[b+1] - cu_M_host[b] tokens (cu_M_host[0] == 0, non-
+ * decreasing; empty prompts allowed).  Keys are packed along the token axis:
+ *
+ *   Q_la      [B, N, L, H, d]
+ *   K_prompt  [L, H_kv, T, d]   T = cu_M_host[B]; prompt b occupies rows cu_M[b]..cu_M[b+1]-1
+ *   K_la      [B, L, H_kv, N, d]
+ *   importance[T]               fp32; entries of prompt b at offsets cu_M[b]..
+ *
+ * Same definition and requirements as sp_score, per prompt. */
+sp_status sp_score_varlen(const void* Q_la, const void* K_prompt, const void* K_la,
+                          int B, const int64_t* cu_M_host,
+                          int L, int H, int H_kv, int d, int N, sp_dtype dtype,
+                          float* importance, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Selection                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes sp_select needs for a prompt of M tokens and this chunk size. */
+size_t sp_select_workspace_size(int64_t M, int chunk);
+
+/* Kept original position IDs of one prompt.
+ *
+ * Token scores x_i are the fp32 importance values as fp64, optionally
+ * normalised and boosted (`boost`, NULL = neither).  Chunks are the contiguous
+ * ranges [c*chunk, min((c+1)*chunk, M)), nc = ceil(M/chunk); a chunk's mean is
+ * its fp64 sum (added left to right) divided by its real size (paper review,
+ * chunk formula; llama.cpp guide, select_chunks).
+ *
+ * SP_SELECT_TOPK (rate = keep_rate, 0 < rate <= 1): chunk means are smoothed
+ * by a stride-1, centred average pool of pool_k chunks (odd; an edge window
+ * averages only its in-range chunks), and exactly kc = max(1,
+ * ceil(f32(nc) * f32(rate))) chunks with the largest pooled score are kept,
+ * ties to the lower chunk index (paper review, "chunk selection and pooling
+ * denoising"; the guide's kc formula).
+ *
+ * SP_SELECT_MASS (rate = tau, 0 < tau <= 1; pool_k must be 1): chunks are
+ * ranked by mean (descending, ties to the lower index) and the shortest ranked
+ * prefix whose running sum of chunk sums (added in ranked order) reaches
+ * tau * total (chunk sums added in chunk order) is kept; all chunks if it never
+ * does (llama.cpp guide, "v3 Improvements: Cumulative Attention Mass
+ * Selection").  Supports nc <= 16384.
+ *
+ *   importance [M] fp32 (finite values)
+ *   kept_pos   [M] int32 output capacity; the first *n_kept entries receive the
+ *              kept tokens' original positions, ascending
+ *   n_kept     device int64 output
+ *
+ * Every fp64 operation follows the fixed order above, so the result is
+ * reproducible bit for bit by any IEEE-754 implementation of the same steps. */
+sp_status sp_select(const float* importance, int64_t M, int chunk, int pool_k, sp_mode mode,
+                    double rate, const sp_boost* boost, int32_t* kept_pos, int64_t* n_kept,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for sp_select_varlen. */
+size_t sp_select_varlen_workspace_size(int B, const int64_t* cu_M_host, int chunk);
+
+/* Per-prompt selection of B packed prompts (importance packed as in
+ * sp_score_varlen).  Prompt b's kept positions (relative to its own start,
+ * i.e. its original position IDs) go to kept_pos[cu_M[b] ...] and its count
+ * to n_kept[b] (device int64[B]).  Same rules as sp_select per prompt. */
+sp_status sp_select_varlen(const float* importance, int B, const int64_t* cu_M_host, int chunk,
+                           int pool_k, sp_mode mode, double rate, const sp_boost* boost,
+                           int32_t* kept_pos, int64_t* n_kept, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `stream` and returns the run-time status a kernel recorded in
+ * the workspace `ws` of the last call that used it: SP_OK, SP_ETIMEOUT (a
+ * bounded wait gave up) or SP_EDEVICE.  Also returns SP_ECUDA if the stream
+ * reports an error. */
+sp_status sp_workspace_status(const void* ws, void* stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* sp_last_error(void);
+
+/* Name of a status code. */
+const char* sp_status_string(sp_status s);
+
+/* ABI version (major * 100 + minor). */
+int sp_version(void);
+
+/* Number of CUDA kernels this process has launched through the library
+ * (all entry points, all threads).  For accounting in benchmarks. */
+uint64_t sp_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECPREFILL_H */

@@ -1,0 +1,422 @@
+// Chunk scoring, pooling, chunk selection and position-ID compaction.
+//
+// Method: paper review "Speculative Prefill ...", chunk formula and section
+// "chunk selection and pooling denoising" (chunk means -> 1D average pool ->
+// top-K chunks) and "position ID recovery" (kept tokens keep their original
+// positions); llama.cpp guide "SpecPrefill -- Implementation Guide", function
+// select_chunks (nc = ceil(M/chunk), kc = max(1, ceil(nc * keep_pct)) with a
+// float product, ascending output), "v3 Improvements" (structural boost,
+// cumulative attention mass) and "v3.1: Score Normalization".
+//
+// Every fp64 step uses explicitly rounded intrinsics (__dadd_rn, __dmul_rn,
+// __ddiv_rn) in a fixed order -- token scores left to right inside a chunk,
+// pooled windows left to right, the total mass in chunk order and the running
+// mass in ranked order -- so the result equals any IEEE-754 evaluation of the
+// same steps bit for bit.
+//
+// Kernels: (0) per-prompt min/max (normalisation only), (1) chunk sums and
+// means, (2) pooled scores (top-K mode), (3) one CTA per prompt: radix select
+// of exactly kc chunks on (score desc, index asc), or a bitonic sort of
+// (mean desc, index asc) and the running-mass cut; then the exclusive scan of
+// kept chunk sizes, (4) compaction of the kept positions.
+#include "sp_common.cuh"
+
+#include <math.h>
+#include <stdint.h>
+
+namespace sp {
+namespace {
+
+constexpr int kMaxBatch = 256;
+constexpr int kSelThreads = 1024;
+constexpr int kMassMaxChunks = 16384;
+
+struct SelGeo {
+    int B, chunk, pool_k;
+    int mode;
+    double rate;
+    int has_boost;
+    int first_n, last_n, normalize;
+    double first_mult, last_mult;
+    int64_t cu[kMaxBatch + 1];      // token offsets
+    int64_t cn[kMaxBatch + 1];      // chunk offsets
+};
+
+// IEEE order of doubles as unsigned integers (+0 and -0 map to the same key).
+__device__ __forceinline__ uint64_t order_key(double v) {
+    if (v == 0.0) v = 0.0;
+    uint64_t u = (uint64_t)__double_as_longlong(v);
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
+__device__ __forceinline__ int find_batch(const int64_t* cu, int B, int64_t x) {
+    int lo = 0, hi = B - 1;                 // largest b with cu[b] <= x
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// (0) min and max importance of each prompt (one CTA per prompt).
+__global__ void __launch_bounds__(1024) minmax_kernel(const SelGeo g, const float* __restrict__ imp,
+                                                      float2* __restrict__ mm) {
+    const int b = blockIdx.x;
+    const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
+    float mn = INFINITY, mx = -INFINITY;
+    for (int64_t i = threadIdx.x; i < Mb; i += blockDim.x) {
+        float v = imp[m0 + i];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+    }
+    __shared__ float smn[32], smx[32];
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if ((threadIdx.x & 31) == 0) { smn[threadIdx.x >> 5] = mn; smx[threadIdx.x >> 5] = mx; }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        int nw = blockDim.x >> 5;
+        mn = threadIdx.x < nw ? smn[threadIdx.x] : INFINITY;
+        mx = threadIdx.x < nw ? smx[threadIdx.x] : -INFINITY;
+        for (int o = 16; o > 0; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        if (threadIdx.x == 0) mm[b] = make_float2(mn, mx);
+    }
+}
+
+// Token score: fp64 importance, optionally normalised and boosted.
+__device__ __forceinline__ double token_score(const SelGeo& g, float v, int64_t i, int64_t Mb,
+                                              float2 mm) {
+    double x = (double)v;
+    if (g.has_boost) {
+        if (g.normalize) {
+            if (mm.y > mm.x)
+                x = __ddiv_rn(__dsub_rn(x, (double)mm.x), __dsub_rn((double)mm.y, (double)mm.x));
+            else
+                x = 1.0;
+        }
+        if (i < (int64_t)g.first_n) x = __dmul_rn(x, g.first_mult);
+        if (i >= Mb - (int64_t)g.last_n) x = __dmul_rn(x, g.last_mult);
+    }
+    return x;
+}
+
+// (1) chunk sums (left to right from 0.0) and means (one divide).
+__global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const float2* __restrict__ mm,
+                             double* __restrict__ sums, double* __restrict__ means) {
+    const int64_t total = g.cn[g.B];
+    for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
+         gc += (int64_t)gridDim.x * blockDim.x) {
+        const int b = find_batch(g.cn, g.B, gc);
+        const int64_t c = gc - g.cn[b];
+        const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
+        const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
+        const float2 mmb = g.has_boost && g.normalize ? mm[b] : make_float2(0.f, 0.f);
+        double s = 0.0;
+        for (int64_t i = lo; i < hi; ++i) s = __dadd_rn(s, token_score(g, imp[m0 + i], i, Mb, mmb));
+        sums[gc] = s;
+        means[gc] = __ddiv_rn(s, (double)(hi - lo));
+    }
+}
+
+// (2) centred average pool over the prompt's own chunks; edges average in-range chunks.
+__global__ void pool_kernel(const SelGeo g, const double* __restrict__ means, double* __restrict__ pooled) {
+    const int64_t total = g.cn[g.B];
+    const int r = (g.pool_k - 1) / 2;
+    for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
+         gc += (int64_t)gridDim.x * blockDim.x) {
+        const int b = find_batch(g.cn, g.B, gc);
+        const int64_t c0 = g.cn[b], nc = g.cn[b + 1] - c0, c = gc - c0;
+        const int64_t lo = c - r < 0 ? 0 : c - r;
+        const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
+        double s = 0.0;
+        for (int64_t t = lo; t <= hi; ++t) s = __dadd_rn(s, means[c0 + t]);
+        pooled[gc] = __ddiv_rn(s, (double)(hi - lo + 1));
+    }
+}
+
+// Block-wide exclusive scan of one 64-bit value per thread; returns the prefix
+// and writes the block total to *total (all threads).
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* sh, long long* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    long long x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        long long s = lane < nw ? sh[lane] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < nw) sh[lane] = s;             // inclusive warp totals
+    }
+    __syncthreads();
+    long long base = w > 0 ? sh[w - 1] : 0;
+    *total = sh[nw - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// (3) per-prompt selection.  Writes keep flags, kept-size offsets and n_kept.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, const double* __restrict__ sums,
+                                                             const double* __restrict__ means,
+                                                             const double* __restrict__ pooled,
+                                                             int* __restrict__ flags,
+                                                             int64_t* __restrict__ offs,
+                                                             int64_t* __restrict__ n_kept) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __shared__ long long scan_sh[32];
+    __shared__ unsigned hist[256];
+    __shared__ uint64_t s_prefix;
+    __shared__ int s_remaining;
+    __shared__ int s_kstar;
+
+    const int b = blockIdx.x;
+    const int64_t c0 = g.cn[b];
+    const int nc = (int)(g.cn[b + 1] - c0);
+    const int64_t Mb = g.cu[b + 1] - g.cu[b];
+    const int tid = threadIdx.x;
+    if (nc == 0) {
+        if (tid == 0) n_kept[b] = 0;
+        return;
+    }
+
+    if (g.mode == SP_SELECT_TOPK) {
+        // kc = max(1, ceil(f32(nc) * f32(keep_rate))), at most nc.
+        const float prod = (float)nc * (float)g.rate;
+        int kc = (int)ceilf(prod);
+        kc = kc < 1 ? 1 : (kc > nc ? nc : kc);
+        // Radix select (8 bits per pass, most significant first) of the kc-th
+        // largest key; afterwards `remaining` keys equal to it must be taken.
+        uint64_t prefix = 0, pmask = 0;
+        int remaining = kc;
+        for (int pass = 0; pass < 8; ++pass) {
+            const int shift = 56 - 8 * pass;
+            for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+            __syncthreads();
+            for (int c = tid; c < nc; c += blockDim.x) {
+                uint64_t k = order_key(pooled[c0 + c]);
+                if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (tid < 32) {
+                // lane covers digits [8*lane, 8*lane+8); count keys with a larger digit.
+                unsigned local = 0;
+                for (int q = 0; q < 8; ++q) local += hist[tid * 8 + q];
+                unsigned above = 0;                   // sum over lanes > tid
+                unsigned x = local;
+                for (int o = 1; o < 32; o <<= 1) {
+                    unsigned y = __shfl_down_sync(0xffffffffu, x, o);
+                    if (tid + o < 32) x += y;
+                }
+                above = x - local;                    // inclusive suffix minus own
+                if (above < (unsigned)remaining && above + local >= (unsigned)remaining) {
+                    unsigned cum = above;
+                    for (int q = 7; q >= 0; --q) {
+                        unsigned hq = hist[tid * 8 + q];
+                        if (cum + hq >= (unsigned)remaining) {
+                            s_prefix = prefix | ((uint64_t)(tid * 8 + q) << shift);
+                            s_remaining = remaining - (int)cum;
+                            break;
+                        }
+                        cum += hq;
+                    }
+                }
+            }
+            __syncthreads();
+            prefix = s_prefix;
+            remaining = s_remaining;
+            pmask |= (0xFFull << shift);
+            __syncthreads();
+        }
+        const uint64_t T = prefix;
+        long long taken_eq = 0, running = 0;
+        for (int base = 0; base < nc; base += blockDim.x) {
+            const int c = base + tid;
+            const bool in = c < nc;
+            const uint64_t k = in ? order_key(pooled[c0 + c]) : 0;
+            const bool gt = in && k > T, eq = in && k == T;
+            long long tot_eq;
+            long long rank = block_exclusive_scan(eq ? 1 : 0, scan_sh, &tot_eq);
+            const bool keep = gt || (eq && taken_eq + rank < remaining);
+            const int64_t lo = (int64_t)c * g.chunk;
+            const long long sz = keep ? (long long)(min(lo + (int64_t)g.chunk, Mb) - lo) : 0;
+            long long tot_sz;
+            long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+            if (in) {
+                flags[c0 + c] = keep ? 1 : 0;
+                offs[c0 + c] = running + off;
+            }
+            taken_eq += tot_eq;
+            running += tot_sz;
+        }
+        if (tid == 0) n_kept[b] = running;
+        return;
+    }
+
+    // Cumulative-mass mode: bitonic sort of (key = descending mean, index).
+    int P = 1;
+    while (P < nc) P <<= 1;
+    uint64_t* keys = reinterpret_cast<uint64_t*>(dsm);
+    int* idx = reinterpret_cast<int*>(dsm + sizeof(uint64_t) * P);
+    for (int i = tid; i < P; i += blockDim.x) {
+        if (i < nc) { keys[i] = ~order_key(means[c0 + i]); idx[i] = i; }
+        else        { keys[i] = ~0ull; idx[i] = 0x7fffffff; }
+    }
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < P / 2; i += blockDim.x) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const uint64_t ka = keys[lo], kb = keys[hi];
+                const int ia = idx[lo], ib = idx[hi];
+                const bool a_gt_b = ka > kb || (ka == kb && ia > ib);
+                if (a_gt_b == up) {
+                    keys[lo] = kb; keys[hi] = ka;
+                    idx[lo] = ib; idx[hi] = ia;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (tid == 0) {
+        double total = 0.0;
+        for (int c = 0; c < nc; ++c) total = __dadd_rn(total, sums[c0 + c]);
+        const double target = __dmul_rn(g.rate, total);
+        double cum = 0.0;
+        int kstar = nc;
+        for (int k = 0; k < nc; ++k) {
+            cum = __dadd_rn(cum, sums[c0 + idx[k]]);
+            if (cum >= target) { kstar = k + 1; break; }
+        }
+        s_kstar = kstar;
+    }
+    __syncthreads();
+    const int kstar = s_kstar;
+    for (int k = tid; k < nc; k += blockDim.x) flags[c0 + idx[k]] = k < kstar ? 1 : 0;
+    __syncthreads();
+    long long running = 0;
+    for (int base = 0; base < nc; base += blockDim.x) {
+        const int c = base + tid;
+        const bool in = c < nc;
+        const bool keep = in && flags[c0 + c] != 0;
+        const int64_t lo = (int64_t)c * g.chunk;
+        const long long sz = keep ? (long long)(min(lo + (int64_t)g.chunk, Mb) - lo) : 0;
+        long long tot_sz;
+        long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        if (in) offs[c0 + c] = running + off;
+        running += tot_sz;
+    }
+    if (tid == 0) n_kept[b] = running;
+}
+
+// (4) every token of a kept chunk writes its original position.
+__global__ void compact_kernel(const SelGeo g, const int* __restrict__ flags,
+                               const int64_t* __restrict__ offs, int32_t* __restrict__ kept_pos) {
+    const int64_t T = g.cu[g.B];
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < T;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int b = find_batch(g.cu, g.B, t);
+        const int64_t m0 = g.cu[b], i = t - m0, c = i / g.chunk;
+        const int64_t gc = g.cn[b] + c;
+        if (flags[gc]) kept_pos[m0 + offs[gc] + (i - c * g.chunk)] = (int32_t)i;
+    }
+}
+
+struct SelLayout {
+    size_t mm, sums, means, pooled, flags, offs, total;
+};
+
+SelLayout sel_layout(const SelectProblem& p) {
+    Carve c;
+    SelLayout lo;
+    const size_t nc = (size_t)std::max<int64_t>(p.total_chunks, 1);
+    lo.mm = c.take(sizeof(float2) * std::max(p.B, 1));
+    lo.sums = c.take(sizeof(double) * nc);
+    lo.means = c.take(sizeof(double) * nc);
+    lo.pooled = c.take(sizeof(double) * nc);
+    lo.flags = c.take(sizeof(int) * nc);
+    lo.offs = c.take(sizeof(int64_t) * nc);
+    lo.total = c.off;
+    return lo;
+}
+
+}  // namespace
+
+size_t select_ws_bytes(const SelectProblem& p) { return sel_layout(p).total; }
+
+sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
+    if (p.B > kMaxBatch) {
+        set_error("sp_select: batch of %d prompts exceeds the supported %d", p.B, kMaxBatch);
+        return SP_EUNSUPPORTED;
+    }
+    if (p.mode == SP_SELECT_MASS && p.max_nc > kMassMaxChunks) {
+        set_error("sp_select: cumulative-mass mode supports at most %d chunks per prompt (got %lld)",
+                  kMassMaxChunks, (long long)p.max_nc);
+        return SP_EUNSUPPORTED;
+    }
+    SelGeo g;
+    g.B = p.B; g.chunk = p.chunk; g.pool_k = p.pool_k; g.mode = (int)p.mode; g.rate = p.rate;
+    g.has_boost = p.has_boost ? 1 : 0;
+    g.first_n = p.boost.first_n; g.last_n = p.boost.last_n; g.normalize = p.boost.normalize;
+    g.first_mult = p.boost.first_mult; g.last_mult = p.boost.last_mult;
+    g.cu[0] = 0; g.cn[0] = 0;
+    for (int b = 0; b < p.B; ++b) {
+        g.cu[b + 1] = p.cu_M_host[b + 1];
+        const int64_t Mb = p.cu_M_host[b + 1] - p.cu_M_host[b];
+        g.cn[b + 1] = g.cn[b] + (Mb + p.chunk - 1) / p.chunk;
+    }
+    g.cu[0] = p.cu_M_host[0];
+    const SelLayout lo = sel_layout(p);
+    char* w = static_cast<char*>(ws);
+    float2* mm = reinterpret_cast<float2*>(w + lo.mm);
+    double* sums = reinterpret_cast<double*>(w + lo.sums);
+    double* means = reinterpret_cast<double*>(w + lo.means);
+    double* pooled = reinterpret_cast<double*>(w + lo.pooled);
+    int* flags = reinterpret_cast<int*>(w + lo.flags);
+    int64_t* offs = reinterpret_cast<int64_t*>(w + lo.offs);
+
+    SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
+    const int64_t total = g.cn[p.B];
+    if (p.has_boost && p.boost.normalize) {
+        minmax_kernel<<<p.B, 1024, 0, st>>>(g, p.importance, mm);
+        SP_LAUNCH_CHECK();
+    }
+    if (total > 0) {
+        const int blocks = (int)std::min<int64_t>((total + 255) / 256, 2048);
+        chunk_kernel<<<blocks, 256, 0, st>>>(g, p.importance, mm, sums, means);
+        SP_LAUNCH_CHECK();
+        if (p.mode == SP_SELECT_TOPK) {
+            pool_kernel<<<blocks, 256, 0, st>>>(g, means, pooled);
+            SP_LAUNCH_CHECK();
+        }
+    }
+    size_t dyn = 0;
+    if (p.mode == SP_SELECT_MASS) {
+        int P = 1;
+        while (P < p.max_nc) P <<= 1;
+        dyn = (sizeof(uint64_t) + sizeof(int)) * (size_t)P;
+    }
+    SP_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)std::max<size_t>(dyn, 0)));
+    select_kernel<<<p.B, kSelThreads, dyn, st>>>(g, sums, means, pooled, flags, offs, p.n_kept);
+    SP_LAUNCH_CHECK();
+    if (p.T > 0) {
+        const int blocks = (int)std::min<int64_t>((p.T + 255) / 256, 4096);
+        compact_kernel<<<blocks, 256, 0, st>>>(g, flags, offs, p.kept_pos);
+        SP_LAUNCH_CHECK();
+    }
+    return SP_OK;
+}
+
+}  // namespace sp

@@ -1,0 +1,120 @@
+"""Scoring parity: sp_score / sp_score_varlen through the C ABI against the fp64
+oracle, element by element, on the seeded workloads (all five at full size)
+and on random shapes with ragged tails and edge cases."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_helpers import check_importance, config_inputs, config_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import torch
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    from speculative_prefill_token_sp_gb300 import build
+    build.build()
+    import speculative_prefill_token_sp_gb300 as m
+    m.lib()
+    return m
+
+
+def run_score(sp, x):
+    import torch
+    Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
+    imp = sp.score(Q, K, Kla)
+    torch.cuda.synchronize()
+    return imp.cpu().numpy()
+
+
+@pytest.mark.parametrize("index", [0, 1, 2, 3])
+def test_config_parity(sp, index):
+    x = config_inputs(index)
+    got = run_score(sp, x)
+    ref = config_oracle(index)
+    check_importance(got, ref, x.wl.dtype, x.wl.name)
+
+
+def test_varlen_config_parity(sp):
+    import torch
+    v = config_inputs(4)
+    Q, K, Kla, cu = v.packed()
+    got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    refs = config_oracle(4)
+    for b, r in enumerate(v.requests):
+        ref = refs[b]
+        check_importance(got[cu[b]:cu[b + 1]], ref, v.wl.dtype, f"{v.wl.name} request {b}")
+
+
+SHAPES = [
+    # (L, H, H_kv, d, M, N, dtype)
+    (1, 1, 1, 64, 1, 1, "bf16"),
+    (1, 2, 1, 64, 7, 2, "f32"),
+    (2, 4, 2, 128, 129, 3, "bf16"),
+    (3, 8, 8, 64, 300, 1, "bf16"),
+    (2, 8, 1, 128, 1000, 8, "bf16"),
+    (1, 16, 2, 256, 257, 4, "f32"),
+    (2, 6, 3, 72, 513, 5, "bf16"),
+    (1, 32, 4, 128, 4097, 8, "bf16"),
+    (2, 4, 4, 8, 77, 16, "f32"),
+    (1, 64, 1, 64, 200, 4, "bf16"),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "L{}H{}Hkv{}d{}M{}N{}{}".format(*s))
+def test_random_shapes(sp, shape):
+    L, H, H_kv, d, M, N, dt = shape
+    wl = W.Workload("t", L=L, H=H, H_kv=H_kv, d=d, M=M, N=N, dtype=dt, chunk=16, pool_k=3, mode="topk",
+                    keep_rate=0.3, needle_frac=0.05, run_min=2, run_max=8)
+    x = W.make_inputs(wl, seed=1000 + M)
+    got = run_score(sp, x)
+    ref = oracle.importance(x.Q_la, x.K_prompt, x.K_la)
+    check_importance(got, ref, dt, str(shape))
+
+
+def test_varlen_ragged_with_empty_prompts(sp):
+    import torch
+    wl = W.Workload("t", L=2, H=8, H_kv=2, d=64, M=0, N=4, dtype="bf16", chunk=16, pool_k=1, mode="mass",
+                    mass=0.85, needle_frac=0.05, run_min=2, run_max=8)
+    v = W.make_varlen_inputs(wl, 77, lengths=[300, 0, 1, 129, 1000, 0])
+    Q, K, Kla, cu = v.packed()
+    got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    for b, r in enumerate(v.requests):
+        if r.M:
+            check_importance(got[cu[b]:cu[b + 1]], oracle.importance(r.Q_la, r.K_prompt, r.K_la), "bf16", f"req {b}")
+
+
+def test_zero_lookahead_gives_ones_and_empty_prompt_is_noop(sp):
+    import torch
+    K = torch.randn(2, 2, 50, 64, device="cuda").to(torch.bfloat16)
+    Q = torch.empty(0, 2, 4, 64, device="cuda", dtype=torch.bfloat16)
+    Kla = torch.empty(2, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    imp = sp.score(Q, K, Kla)
+    torch.cuda.synchronize()
+    assert torch.all(imp == 1.0)
+    K0 = torch.empty(2, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    Q1 = torch.randn(3, 2, 4, 64, device="cuda").to(torch.bfloat16)
+    Kla1 = torch.randn(2, 2, 3, 64, device="cuda").to(torch.bfloat16)
+    imp = sp.score(Q1, K0, Kla1)
+    torch.cuda.synchronize()
+    assert imp.numel() == 0
+
+
+def test_workspace_status_ok_after_call(sp):
+    import torch
+    x = W.make_config_inputs(0)
+    Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
+    wl = x.wl
+    need = sp.sp_score_workspace_size(wl.L, wl.H, wl.H_kv, wl.d, wl.M, wl.N, sp.SP_F32)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device="cuda")     # garbage workspace
+    imp = torch.empty(wl.M, device="cuda")
+    assert sp.sp_score(Q, K, Kla, wl.L, wl.H, wl.H_kv, wl.d, wl.M, wl.N, sp.SP_F32, imp, ws, need) == sp.SP_OK
+    assert sp.sp_workspace_status(ws) == sp.SP_OK
+    check_importance(imp.cpu().numpy(), oracle.importance(x.Q_la, x.K_prompt, x.K_la), "f32", "garbage ws")
