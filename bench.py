@@ -42,6 +42,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=2, help="workload index (default 2: 8B shape, M=32K)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bare", action="store_true",
+                    help="run only the warm-up and timed steps and print their time (for profilers)")
     return ap.parse_args(argv)
 
 
@@ -308,6 +310,17 @@ def run_gpu(args) -> None:
     st = sp.sp_workspace_status(ws_s, stream)
     if st != sp.SP_OK:
         raise sp.SpError(st, sp.sp_last_error())
+    if args.bare:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"bare": True, "workload": wl.name, "steps": args.steps,
+                              "ms_per_step": e0.elapsed_time(e1) / args.steps}), flush=True)
+        return
 
     # -------- timed region: K steps, L2 flushed between steps --------
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
