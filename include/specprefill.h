@@ -180,6 +180,29 @@ sp_status sp_select_varlen(const float* importance, int B, const int64_t* cu_M_h
                            int32_t* kept_pos, int64_t* n_kept, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* sp_select for callers that cannot allocate device memory.  The method's
+ * pages have no counterpart to this entry point; it exists for deployment.
+ *
+ * Who needs it: code that runs inside a device-memory allocator or its
+ * out-of-memory handler (allocating there would re-enter the allocator),
+ * serving loops whose latency budget forbids cudaMalloc (it can synchronise
+ * the whole device), and plug-ins that a host framework hands only input and
+ * output buffers.  The caller passes inputs and outputs exactly as for
+ * sp_select; the scratch lives in a fixed 3 MiB array of device memory inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated or freed.
+ *
+ * Limits: one prompt, at most 65536 chunks (ceil(M / chunk)); larger requests
+ * return SP_EUNSUPPORTED before any work is enqueued.  All calls on a device
+ * share the array and leave their contents behind: calls whose work may
+ * overlap on the GPU (e.g. on two unordered streams) race and must not be
+ * issued.  The first call on each device looks up the array's address with
+ * that device current; make it before any stream capture.  Results are
+ * identical to sp_select's. */
+sp_status sp_select_noalloc(const float* importance, int64_t M, int chunk, int pool_k, sp_mode mode,
+                            double rate, const sp_boost* boost, int32_t* kept_pos, int64_t* n_kept,
+                            void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                   */
 /* ------------------------------------------------------------------------ */

@@ -19,7 +19,8 @@ __all__ = [
     "SP_BF16", "SP_F32", "SP_SELECT_TOPK", "SP_SELECT_MASS", "SpBoost", "SpError", "lib", "lib_path",
     "sp_score_workspace_size", "sp_score", "sp_score_varlen_workspace_size", "sp_score_varlen",
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
-    "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version", "sp_kernel_launches",
+    "sp_select_noalloc", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
+    "sp_kernel_launches",
     "score", "score_varlen", "select", "select_varlen", "V3_BOOST",
 ]
 
@@ -61,6 +62,7 @@ _SIGS = {
     "sp_select": (_i32, [_vp, _i64, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sp_select_varlen_workspace_size": (_sz, [_i32, _vp, _i32]),
     "sp_select_varlen": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "sp_select_noalloc": (_i32, [_vp, _i64, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp]),
     "sp_workspace_status": (_i32, [_vp, _vp]),
     "sp_last_error": (_c.c_char_p, []),
     "sp_status_string": (_c.c_char_p, [_i32]),
@@ -170,6 +172,12 @@ def sp_select_varlen(importance, B, cu_M_host, chunk, pool_k, mode, rate, boost,
     return lib().sp_select_varlen(_ptr(importance), B, ctypes.addressof(cu), chunk, pool_k, mode, rate,
                                   _boost(boost), _ptr(kept_pos), _ptr(n_kept), _ptr(ws), ws_bytes,
                                   _stream(stream))
+
+
+def sp_select_noalloc(importance, M, chunk, pool_k, mode, rate, boost, kept_pos, n_kept, stream=None) -> int:
+    """sp_select without a workspace (scratch in a fixed device array of the library)."""
+    return lib().sp_select_noalloc(_ptr(importance), M, chunk, pool_k, mode, rate, _boost(boost), _ptr(kept_pos),
+                                   _ptr(n_kept), _stream(stream))
 
 
 def sp_workspace_status(ws, stream=None) -> int:

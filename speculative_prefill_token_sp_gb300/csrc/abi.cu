@@ -223,6 +223,35 @@ sp_status run_select(const char* fn, const SelectProblem& p, void* ws, size_t ws
 
 }  // namespace
 
+namespace sp {
+
+// Validation and problem set-up of sp_select, shared with the entry point in
+// select_noalloc.cu.
+sp_status select_validate_single(const char* fn, const float* importance, int64_t M, int chunk, int pool_k,
+                                 sp_mode mode, double rate, const sp_boost* boost, int32_t* kept_pos,
+                                 int64_t* n_kept, SelectProblem* out, int64_t* cu_storage) {
+    if (M < 0 || M > (int64_t)INT32_MAX) {
+        set_error("%s: M must be in [0, 2^31-1] (got %lld)", fn, (long long)M);
+        return M < 0 ? SP_EINVAL : SP_EUNSUPPORTED;
+    }
+    sp_status s = check_select_params(fn, chunk, pool_k, mode, rate, boost);
+    if (s != SP_OK) return s;
+    if (M > 0 && (!importance || !kept_pos)) {
+        set_error("%s: null importance or kept_pos pointer", fn);
+        return SP_EINVAL;
+    }
+    if (!n_kept) {
+        set_error("%s: null n_kept pointer", fn);
+        return SP_EINVAL;
+    }
+    cu_storage[0] = 0;
+    cu_storage[1] = M;
+    *out = make_select_problem(importance, 1, cu_storage, chunk, pool_k, mode, rate, boost, kept_pos, n_kept);
+    return SP_OK;
+}
+
+}  // namespace sp
+
 extern "C" {
 
 size_t sp_score_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype) {

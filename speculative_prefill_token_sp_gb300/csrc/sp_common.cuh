@@ -70,6 +70,12 @@ struct SelectProblem {
 size_t select_ws_bytes(const SelectProblem& p);
 sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st);
 
+// Argument checks of a single-prompt selection (defined in abi.cu).  On
+// success fills *out; cu_storage (2 entries) must outlive *out.
+sp_status select_validate_single(const char* fn, const float* importance, int64_t M, int chunk, int pool_k,
+                                 sp_mode mode, double rate, const sp_boost* boost, int32_t* kept_pos,
+                                 int64_t* n_kept, SelectProblem* out, int64_t* cu_storage);
+
 #define SP_CUDA_TRY(expr)                                                          \
     do {                                                                           \
         cudaError_t _e = (expr);                                                   \
