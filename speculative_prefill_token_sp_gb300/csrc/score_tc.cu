@@ -1,8 +1,748 @@
-// Tensor-core (tcgen05 + TMA) scoring path -- placeholder until it lands.
+// Look-ahead attention importance on GB300 tensor cores: tcgen05.mma + TMA + TMEM.
+//
+// Method (paper review "Speculative Prefill ...", core formulas; llama.cpp
+// guide "SpecPrefill -- Implementation Guide", Token Importance):
+//   s[l,h,j,i]    = Q_la[j,l,h] . K[l,g,i] / sqrt(d)
+//   lse[l,h,j]    = log(sum_i exp(s) + sum_{k<=j} exp(u_k))    (causal look-ahead keys u)
+//   importance[i] = (1/N) sum_j max_{l,h} exp(s[l,h,j,i] - lse[l,h,j])
+// computed as (1/N) sum_j exp(max_{l,h}(s - lse)) (exp is increasing).
+//
+// Design (one persistent CTA per SM, cooperative launch so that all CTAs are
+// resident):
+//  * every CTA owns one fixed range of prompt tokens (multiples of 32) in every
+//    (layer, KV head) slab, so the max over heads and layers of a token stays
+//    inside one CTA: no atomics, and importance is written once;
+//  * warp 0 streams the CTA's K rows of slab after slab with TMA (32-row x
+//    128-byte boxes, 128B swizzle) through a ring of shared-memory stages, and
+//    the slab's query rows (a pre-swizzled image built by tc_prep_kernel) with
+//    one bulk copy;
+//  * warp 1 issues tcgen05.mma (M = 128 tokens, N = 32 query rows = N*G padded,
+//    K = 16 per instruction, bf16 in, fp32 accumulate) into TMEM; each slab
+//    gets one TMEM slot that holds all of the CTA's logits of that slab;
+//  * warps 2-5 (128 threads, one TMEM lane each) read the logits back, reduce
+//    per-row softmax statistics over the CTA's tokens and publish them; the last
+//    CTA to finish a slab merges all partial statistics with the look-ahead keys
+//    into lse and raises the slab's ready flag;
+//  * lag slabs later the same warps re-read the slab's logits from TMEM (not
+//    HBM), subtract lse, take the max over the G heads of each look-ahead step
+//    and fold it into a per-token running max kept in shared memory; the TMEM
+//    slot is then released to the MMA warp.
+// K is therefore read exactly once from HBM and the contraction runs once.
+//
+// Every wait is bounded (mbarrier phases, the cross-CTA ready flags): on
+// timeout the kernel records SP_ETIMEOUT in the workspace header, all roles
+// stop, in-flight copies and MMAs are waited for (again bounded) and TMEM is
+// freed before the CTA exits.
 #include "sp_common.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
 namespace sp {
-bool score_tc_supported(const ScoreProblem&) { return false; }
-size_t score_tc_ws_bytes(const ScoreProblem&) { return 0; }
-sp_status score_tc_launch(const ScoreProblem&, void*, cudaStream_t) { return SP_EUNSUPPORTED; }
+namespace {
+
+constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue (128 threads)
+constexpr int kTileRows = 128;       // tokens per MMA tile (MMA M)
+constexpr int kBoxRows = 32;         // rows per TMA box
+constexpr int kUnit = 32;            // token-range granularity
+constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
+constexpr int kMaxCtas = 256;
+constexpr int kMaxTiles = 8;         // tiles per CTA per slab
+constexpr int kMaxSlots = 8;
+constexpr int kSmemBudget = 227 * 1024;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
+
+struct TcParams {
+    int L, H, H_kv, G, N, R, d;
+    int S;              // slabs = L * H_kv
+    int P;              // CTAs
+    int U;              // 32-token units of the prompt
+    int n_tiles_max, slot_cols, NS, lag, tmem_cols, stages;
+    int64_t T;          // rows per slab in K (= M for one prompt)
+    float scale, scale_log2e;
+    // shared-memory carve (byte offsets from the 1024-aligned base)
+    int off_q, off_s, off_acc, off_lse, off_bar, smem_bytes;
+    // workspace
+    const uint8_t* qimg;    // [S][kRP * d] bf16, 128B-swizzled image of the slab's query rows
+    const float2* la;       // [S][kRP] softmax statistics of the look-ahead keys
+    float2* partials;       // [S][P][kRP]
+    float* lse;             // [S][kRP]
+    unsigned* cnt;          // [S] CTAs done with a slab's statistics
+    unsigned* ready;        // [S] lse published
+    WsHeader* hdr;
+    float* importance;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Returns false if the
+// kernel is aborting or the wait timed out (then the abort flag is raised).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr, int where) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((i & 63u) == 0) {
+            unsigned long long t = global_ns();
+            if (i == 0) t0 = t;
+            else if (t - t0 > kTimeoutNs) {
+                record_error(hdr, SP_ETIMEOUT, where);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);     // start address
+    d |= (uint64_t)1u << 16;                      // leading-dimension byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024u >> 4) << 32;            // stride-dimension byte offset
+    d |= (uint64_t)1u << 46;                      // descriptor version
+    d |= (uint64_t)2u << 61;                      // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (K-major),
+// fp32 accumulator, M = 128, N = n.
+__host__ __device__ constexpr uint32_t instr_desc_bf16(int n) {
+    return (1u << 4)                    // accumulator format: f32
+           | (1u << 7)                  // A format: bf16
+           | (1u << 10)                 // B format: bf16
+           | ((uint32_t)(n >> 3) << 17) // N / 8
+           | ((uint32_t)(128 >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Merge softmax statistics (m2, z2) into (m, z) (natural-log domain).
+__device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) { m = m2; z = z2; return; }
+    const float mx = fmaxf(m, m2);
+    z = z * __expf(m - mx) + z2 * __expf(m2 - mx);
+    m = mx;
+}
+
+// ---------------------------------------------------------------------------
+// Per-call preparation: swizzled query images and look-ahead statistics.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __nv_bfloat16* __restrict__ Q,
+                                                      const __nv_bfloat16* __restrict__ Kla,
+                                                      uint8_t* __restrict__ qimg, float2* __restrict__ la) {
+    const int s = blockIdx.x;
+    const int l = s / p.H_kv, g = s % p.H_kv;
+    const int cpr = p.d / 8;                      // 16-byte chunks per row
+    uint8_t* img = qimg + (size_t)s * kRP * p.d * 2;
+    for (int idx = threadIdx.x; idx < kRP * cpr; idx += blockDim.x) {
+        const int r = idx / cpr, ch = idx % cpr;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.R) {
+            const int j = r / p.G, h = g * p.G + r % p.G;
+            v = *reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d + ch * 8);
+        }
+        const int half = ch >> 3, c = ch & 7;
+        const size_t off = (size_t)half * (kRP * 128) + (size_t)r * 128 + (size_t)((c ^ (r & 7)) * 16);
+        *reinterpret_cast<uint4*>(img + off) = v;
+    }
+    for (int r = threadIdx.x; r < kRP; r += blockDim.x) {
+        float m = -INFINITY, z = 0.f;
+        if (r < p.R) {
+            const int j = r / p.G, h = g * p.G + r % p.G;
+            const __nv_bfloat16* q = Q + (((size_t)j * p.L + l) * p.H + h) * p.d;
+            for (int k = 0; k <= j; ++k) {
+                const __nv_bfloat16* kk = Kla + (((size_t)l * p.H_kv + g) * p.N + k) * p.d;
+                float u = 0.f;
+                for (int t = 0; t < p.d; ++t) u = fmaf(__bfloat162float(q[t]), __bfloat162float(kk[t]), u);
+                merge(m, z, u * p.scale, 1.f);
+            }
+        }
+        la[(size_t)s * kRP + r] = make_float2(m, z);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The persistent scoring kernel
+// ---------------------------------------------------------------------------
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kHalves = D / 64;
+    constexpr int kStageBytes = kTileRows * D * 2;
+    constexpr int kQBytes = kRP * D * 2;
+    constexpr uint32_t kIdesc = instr_desc_bf16(kRP);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    // this CTA's token range [t_begin, t_end) of every slab
+    const int u0 = (int)(((int64_t)c * p.U) / p.P), u1 = (int)(((int64_t)(c + 1) * p.U) / p.P);
+    const int64_t t_begin = (int64_t)u0 * kUnit;
+    const int64_t t_end = min((int64_t)u1 * kUnit, p.T);
+    const int len = (int)(t_end - t_begin);
+    const int n_tiles = (len + kTileRows - 1) / kTileRows;
+
+    uint8_t* k_stage = smem;                                   // [stages][kStageBytes]
+    uint8_t* q_buf = smem + p.off_q;                           // [2][kQBytes]
+    float* S = reinterpret_cast<float*>(smem + p.off_s);       // [kRP][4][33]
+    float* acc = reinterpret_cast<float*>(smem + p.off_acc);   // [n_tiles_max][N][128]
+    float* lse_s = reinterpret_cast<float*>(smem + p.off_lse); // [kRP]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = bars + p.stages;
+    uint64_t* q_full = bars + 2 * p.stages;
+    uint64_t* q_empty = q_full + 2;
+    uint64_t* slot_full = q_empty + 2;
+    uint64_t* slot_empty = slot_full + kMaxSlots;
+    uint64_t* final_bar = slot_empty + kMaxSlots;
+    volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(final_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+    volatile int* last_flag = abort_flag + 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(smem_u32(&k_full[i]), 1);
+            mbar_init(smem_u32(&k_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&q_full[i]), 1);
+            mbar_init(smem_u32(&q_empty[i]), 1);
+        }
+        for (int i = 0; i < kMaxSlots; ++i) {
+            mbar_init(smem_u32(&slot_full[i]), 1);
+            mbar_init(smem_u32(&slot_empty[i]), 1);
+        }
+        mbar_init(smem_u32(final_bar), 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32((const void*)tmem_base_sh)), "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // running max of (s - lse) over (layer, head), per token and look-ahead step
+    for (int i = threadIdx.x; i < p.n_tiles_max * p.N * kTileRows; i += kThreads) acc[i] = -INFINITY;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_sh;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int s = 0; s < p.S && ok; ++s) {
+                const int qb = s & 1;
+                if (s >= 2) ok = mbar_wait(smem_u32(&q_empty[qb]), ((s >> 1) - 1) & 1, abort_flag, p.hdr, 1);
+                if (!ok) break;
+                mbar_expect_tx(smem_u32(&q_full[qb]), kQBytes);
+                bulk_load(smem_u32(q_buf + qb * kQBytes), p.qimg + (size_t)s * kQBytes, kQBytes,
+                          smem_u32(&q_full[qb]));
+                const int64_t row0 = (int64_t)s * p.T + t_begin;
+                for (int t = 0; t < n_tiles; ++t, ++it) {
+                    const int st = it % p.stages;
+                    if (it >= p.stages) ok = mbar_wait(smem_u32(&k_empty[st]), ((it / p.stages) - 1) & 1, abort_flag, p.hdr, 2);
+                    if (!ok) break;
+                    const int rows = min(kTileRows, len - t * kTileRows);
+                    const int nbox = (rows + kBoxRows - 1) / kBoxRows;
+                    mbar_expect_tx(smem_u32(&k_full[st]), (uint32_t)(nbox * kBoxRows * D * 2));
+                    uint8_t* dst = k_stage + (size_t)st * kStageBytes;
+                    for (int hf = 0; hf < kHalves; ++hf)
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(smem_u32(dst + hf * (kTileRows * 128) + b * (kBoxRows * 128)), &kmap,
+                                        hf * 64, (int)(row0 + t * kTileRows + b * kBoxRows), smem_u32(&k_full[st]));
+                }
+            }
+            // wait (bounded) for every copy still in flight before the CTA may exit
+            for (int j = max(0, it - p.stages); j < it; ++j) {
+                const unsigned long long t0 = global_ns();
+                while (!mbar_try_wait(smem_u32(&k_full[j % p.stages]), (j / p.stages) & 1))
+                    if (global_ns() - t0 > kTimeoutNs) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int s = 0; s < p.S && ok; ++s) {
+                const int slot = s % p.NS;
+                if (s >= p.NS) ok = mbar_wait(smem_u32(&slot_empty[slot]), ((s / p.NS) - 1) & 1, abort_flag, p.hdr, 3);
+                if (!ok) break;
+                tc_fence_after();
+                const int qb = s & 1;
+                ok = mbar_wait(smem_u32(&q_full[qb]), (s >> 1) & 1, abort_flag, p.hdr, 4);
+                if (!ok) break;
+                const uint32_t qaddr = smem_u32(q_buf + qb * kQBytes);
+                for (int t = 0; t < n_tiles; ++t, ++it) {
+                    const int st = it % p.stages;
+                    ok = mbar_wait(smem_u32(&k_full[st]), (it / p.stages) & 1, abort_flag, p.hdr, 5);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(k_stage + (size_t)st * kStageBytes);
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(slot * p.slot_cols + t * kRP);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int hf = kk >> 2, ko = kk & 3;
+                        const uint64_t a = smem_desc(kaddr + hf * (kTileRows * 128) + ko * 32);
+                        const uint64_t b = smem_desc(qaddr + hf * (kRP * 128) + ko * 32);
+                        tc_mma(d_tmem, a, b, kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&k_empty[st]));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&q_empty[qb]));
+                tc_commit(smem_u32(&slot_full[slot]));
+            }
+            // all MMAs issued so far complete before TMEM may be freed
+            tc_commit(smem_u32(final_bar));
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(smem_u32(final_bar), 0))
+                if (global_ns() - t0 > kTimeoutNs) break;
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int e = threadIdx.x - 64;                // 0..127
+        const int quad = warp & 3;                     // TMEM lane quadrant of this warp
+        const int tok = quad * 32 + lane;              // token row inside a tile
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const int r_e = e >> 2, part = e & 3;          // reduction role: row r_e, quarter `part`
+        bool ok = true;
+        for (int step = 0; step < p.S + p.lag && ok; ++step) {
+            // ---- statistics of slab `step` ----
+            if (step < p.S) {
+                const int s = step, slot = s % p.NS;
+                if (e == 0) mbar_wait(smem_u32(&slot_full[slot]), (s / p.NS) & 1, abort_flag, p.hdr, 6);
+                epi_sync();
+                if (*abort_flag) { ok = false; break; }
+                tc_fence_after();
+                float m_run = -INFINITY, z_run = 0.f;
+                for (int t = 0; t < n_tiles; ++t) {
+                    float x[32];
+                    tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
+                    const bool valid = t * kTileRows + tok < len;
+#pragma unroll
+                    for (int r = 0; r < kRP; ++r) S[(r * 4 + quad) * 33 + lane] = valid ? x[r] : -INFINITY;
+                    epi_sync();
+                    const float* row = S + (r_e * 4 + part) * 33;
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, row[i]);
+                    float z = 0.f;
+                    if (mx != -INFINITY) {
+                        const float off = mx * p.scale_log2e;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) z += exp2f(fmaf(row[i], p.scale_log2e, -off));
+                    }
+                    float m = mx == -INFINITY ? -INFINITY : mx * p.scale;
+#pragma unroll
+                    for (int o = 1; o <= 2; o <<= 1) {
+                        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                        const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+                        merge(m, z, m2, z2);
+                    }
+                    merge(m_run, z_run, m, z);
+                    epi_sync();
+                }
+                if (part == 0) p.partials[((size_t)s * p.P + c) * kRP + r_e] = make_float2(m_run, z_run);
+                __threadfence();
+                epi_sync();
+                if (e == 0) {
+                    const unsigned prev = atomicAdd(&p.cnt[s], 1u);
+                    *last_flag = (prev == (unsigned)p.P - 1u) ? 1 : 0;
+                }
+                epi_sync();
+                if (*last_flag) {
+                    // the last CTA to finish slab s merges every CTA's statistics into lse
+                    __threadfence();
+                    float m = -INFINITY, z = 0.f;
+                    for (int cc = part; cc < p.P; cc += 4) {
+                        const float2 v = __ldcg(&p.partials[((size_t)s * p.P + cc) * kRP + r_e]);
+                        merge(m, z, v.x, v.y);
+                    }
+#pragma unroll
+                    for (int o = 1; o <= 2; o <<= 1) {
+                        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                        const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+                        merge(m, z, m2, z2);
+                    }
+                    if (part == 0) {
+                        const float2 v = __ldcg(&p.la[(size_t)s * kRP + r_e]);
+                        merge(m, z, v.x, v.y);
+                        p.lse[(size_t)s * kRP + r_e] = m + __logf(z);
+                    }
+                    __threadfence();
+                    epi_sync();
+                    if (e == 0) st_release(&p.ready[s], 1u);
+                }
+            }
+            // ---- normalise + max of slab `step - lag` ----
+            if (step >= p.lag) {
+                const int s = step - p.lag, slot = s % p.NS;
+                if (e == 0) {
+                    const unsigned long long t0 = global_ns();
+                    unsigned i = 0;
+                    while (ld_acquire(&p.ready[s]) == 0u) {
+                        if (*abort_flag) break;
+                        if ((++i & 15u) == 0 && global_ns() - t0 > kTimeoutNs) {
+                            record_error(p.hdr, SP_ETIMEOUT, 100 + (s & 0xFF));
+                            *abort_flag = 1;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+                epi_sync();
+                if (*abort_flag) { ok = false; break; }
+                if (e < kRP) lse_s[e] = __ldcg(&p.lse[(size_t)s * kRP + e]);
+                epi_sync();
+                tc_fence_after();
+                for (int t = 0; t < n_tiles; ++t) {
+                    float x[32];
+                    tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
+                    float* a = acc + (size_t)t * p.N * kTileRows + tok;
+#pragma unroll
+                    for (int j = 0; j < kRP / G; ++j) {
+                        if (j < p.N) {
+                            float y = -INFINITY;
+#pragma unroll
+                            for (int hh = 0; hh < G; ++hh)
+                                y = fmaxf(y, fmaf(x[j * G + hh], p.scale, -lse_s[j * G + hh]));
+                            a[j * kTileRows] = fmaxf(a[j * kTileRows], y);
+                        }
+                    }
+                }
+                tc_fence_before();
+                epi_sync();
+                if (e == 0) mbar_arrive(smem_u32(&slot_empty[slot]));
+            }
+        }
+        if (ok) {
+            // importance of this CTA's tokens: (1/N) sum_j exp(max_{l,h}(s - lse))
+            const float inv_n = 1.0f / (float)p.N;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int i = t * kTileRows + tok;
+                if (i < len) {
+                    const float* a = acc + (size_t)t * p.N * kTileRows + tok;
+                    float sum = 0.f;
+                    for (int j = 0; j < p.N; ++j) sum += expf(a[j * kTileRows]);
+                    p.importance[t_begin + i] = sum * inv_n;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+struct Plan {
+    TcParams p;
+    size_t off_qimg, off_la, off_partials, off_lse, off_cnt, off_ready, total;
+};
+
+int sm_count_or(int fallback) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return fallback; }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fallback;
+    }
+    return n;
+}
+
+bool shape_ok(const ScoreProblem& q) {
+    if (q.dtype != SP_BF16 || q.B != 1 || q.N < 1) return false;
+    if (q.d != 64 && q.d != 128) return false;
+    const int G = q.H / q.H_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+    if (q.N * G > kRP) return false;
+    if (q.T < 1 || q.T > (int64_t)INT32_MAX / 4) return false;
+    if ((int64_t)q.L * q.H_kv * q.T > (int64_t)INT32_MAX) return false;   // TMA row coordinate
+    return true;
+}
+
+// Plan for P CTAs; returns false if the problem does not fit this path.
+bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
+    if (!shape_ok(q)) return false;
+    TcParams& p = out.p;
+    p.L = q.L; p.H = q.H; p.H_kv = q.H_kv; p.G = q.H / q.H_kv; p.N = q.N; p.R = q.N * p.G; p.d = q.d;
+    p.S = q.L * q.H_kv;
+    p.T = q.T;
+    p.U = (int)((q.T + kUnit - 1) / kUnit);
+    p.P = std::max(1, std::min(std::min(P_hint, p.U), kMaxCtas));
+    const int units_max = (p.U + p.P - 1) / p.P;
+    p.n_tiles_max = (units_max * kUnit + kTileRows - 1) / kTileRows;
+    if (p.n_tiles_max > kMaxTiles) return false;
+    p.slot_cols = p.n_tiles_max * kRP;
+    p.NS = std::min(kMaxSlots, 512 / p.slot_cols);
+    if (p.NS < 2) return false;
+    p.lag = p.NS - 1;
+    int cols = 32;
+    while (cols < p.NS * p.slot_cols) cols <<= 1;
+    p.tmem_cols = cols;
+    p.scale = 1.0f / sqrtf((float)q.d);
+    p.scale_log2e = p.scale * 1.4426950408889634f;
+    const int stage_bytes = kTileRows * q.d * 2;
+    p.stages = q.d == 128 ? 4 : 8;
+    int off = p.stages * stage_bytes;
+    p.off_q = off;
+    off += 2 * kRP * q.d * 2;
+    p.off_s = off;
+    off += kRP * 4 * 33 * 4;
+    p.off_acc = off;
+    off += p.n_tiles_max * p.N * kTileRows * 4;
+    p.off_lse = off;
+    off += kRP * 4;
+    off = (off + 15) & ~15;
+    p.off_bar = off;
+    off += (2 * p.stages + 4 + 2 * kMaxSlots + 1) * 8 + 16;
+    p.smem_bytes = off + 1024;                    // slack for 1024-byte alignment
+    if (p.smem_bytes > kSmemBudget) return false;
+    // workspace (after the 256-byte header)
+    Carve cv;
+    const size_t S = (size_t)p.S;
+    out.off_qimg = cv.take(S * kRP * q.d * 2);
+    out.off_la = cv.take(S * kRP * sizeof(float2));
+    out.off_partials = cv.take(S * kMaxCtas * kRP * sizeof(float2));
+    out.off_lse = cv.take(S * kRP * sizeof(float));
+    out.off_cnt = cv.take(S * sizeof(unsigned));
+    out.off_ready = cv.take(S * sizeof(unsigned));
+    out.total = cv.off;
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+template <int D, int G>
+sp_status launch_kernel(const CUtensorMap& map, const TcParams& p, cudaStream_t st) {
+    auto kern = tc_score_kernel<D, G>;
+    SP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes));
+    int per_sm = 0;
+    SP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, p.smem_bytes));
+    if (per_sm < 1) {
+        set_error("sp_score: the tensor-core kernel does not fit on an SM (%d bytes of shared memory)", p.smem_bytes);
+        return SP_EUNSUPPORTED;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, p);
+    count_launch();
+    if (e != cudaSuccess) {
+        set_error("sp_score: cooperative launch of %d CTAs failed: %s", p.P, cudaGetErrorString(e));
+        return SP_ECUDA;
+    }
+    return SP_OK;
+}
+
+}  // namespace
+
+bool score_tc_supported(const ScoreProblem& q) {
+    Plan plan;
+    return make_plan(q, sm_count_or(148), plan);
+}
+
+size_t score_tc_ws_bytes(const ScoreProblem& q) {
+    Plan plan;
+    return make_plan(q, kMaxCtas, plan) ? plan.total : 0;
+}
+
+sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
+    Plan plan;
+    const int sms = sm_count_or(0);
+    if (sms < 1 || !make_plan(q, sms, plan)) {
+        set_error("sp_score: shape outside the tensor-core path");
+        return SP_EUNSUPPORTED;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) {
+        set_error("sp_score: cuTensorMapEncodeTiled is unavailable from the driver");
+        return SP_ECUDA;
+    }
+    TcParams& p = plan.p;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.hdr = reinterpret_cast<WsHeader*>(w);
+    p.qimg = w + plan.off_qimg;
+    p.la = reinterpret_cast<const float2*>(w + plan.off_la);
+    p.partials = reinterpret_cast<float2*>(w + plan.off_partials);
+    p.lse = reinterpret_cast<float*>(w + plan.off_lse);
+    p.cnt = reinterpret_cast<unsigned*>(w + plan.off_cnt);
+    p.ready = reinterpret_cast<unsigned*>(w + plan.off_ready);
+    p.importance = q.importance;
+
+    // K viewed as a 2D tensor of L*H_kv*T rows by d bf16 columns; 32-row x 64-column boxes.
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)q.d, (cuuint64_t)p.S * (cuuint64_t)q.T};
+    const cuuint64_t gstride[1] = {(cuuint64_t)q.d * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kBoxRows};
+    const cuuint32_t estride[2] = {1u, 1u};
+    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q.K), gdim, gstride, box,
+                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        set_error("sp_score: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+        return SP_ECUDA;
+    }
+
+    SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
+    SP_CUDA_TRY(cudaMemsetAsync(w + plan.off_cnt, 0, plan.total - plan.off_cnt, st));
+    tc_prep_kernel<<<p.S, 256, 0, st>>>(p, static_cast<const __nv_bfloat16*>(q.Q),
+                                        static_cast<const __nv_bfloat16*>(q.Kla), w + plan.off_qimg,
+                                        reinterpret_cast<float2*>(w + plan.off_la));
+    SP_LAUNCH_CHECK();
+
+    switch (q.d * 16 + p.G) {
+        case 64 * 16 + 1: return launch_kernel<64, 1>(map, p, st);
+        case 64 * 16 + 2: return launch_kernel<64, 2>(map, p, st);
+        case 64 * 16 + 4: return launch_kernel<64, 4>(map, p, st);
+        case 64 * 16 + 8: return launch_kernel<64, 8>(map, p, st);
+        case 128 * 16 + 1: return launch_kernel<128, 1>(map, p, st);
+        case 128 * 16 + 2: return launch_kernel<128, 2>(map, p, st);
+        case 128 * 16 + 4: return launch_kernel<128, 4>(map, p, st);
+        case 128 * 16 + 8: return launch_kernel<128, 8>(map, p, st);
+        default: break;
+    }
+    set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, p.G);
+    return SP_EUNSUPPORTED;
+}
+
 }  // namespace sp

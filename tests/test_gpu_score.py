@@ -38,6 +38,18 @@ def test_config_parity(sp, index):
     check_importance(got, ref, x.wl.dtype, x.wl.name)
 
 
+def test_tensor_core_path_serves_the_8b_workloads(sp):
+    """The 8B-shaped bf16 prompts run on the tcgen05 path: one preparation
+    kernel plus one persistent kernel per call (the general path launches 4)."""
+    import torch
+    x = config_inputs(1)
+    Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
+    n0 = sp.sp_kernel_launches()
+    sp.score(Q, K, Kla)
+    torch.cuda.synchronize()
+    assert sp.sp_kernel_launches() - n0 == 2
+
+
 def test_varlen_config_parity(sp):
     import torch
     v = config_inputs(4)
