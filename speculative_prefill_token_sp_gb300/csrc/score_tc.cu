@@ -8,31 +8,36 @@
 // computed as (1/N) sum_j exp(max_{l,h}(s - lse)) (exp is increasing).
 //
 // Design (one persistent CTA per SM, cooperative launch so that all CTAs are
-// resident):
-//  * every CTA owns one fixed range of prompt tokens (multiples of 32) in every
-//    (layer, KV head) slab, so the max over heads and layers of a token stays
-//    inside one CTA: no atomics, and importance is written once;
-//  * warp 0 streams the CTA's K rows of slab after slab with TMA (32-row x
-//    128-byte boxes, 128B swizzle) through a ring of shared-memory stages, and
-//    the slab's query rows (a pre-swizzled image built by tc_prep_kernel) with
-//    one bulk copy;
-//  * warp 1 issues tcgen05.mma (M = 128 tokens, N = 32 query rows = N*G padded,
-//    K = 16 per instruction, bf16 in, fp32 accumulate) into TMEM; each slab
-//    gets one TMEM slot that holds all of the CTA's logits of that slab;
-//  * warps 2-5 (128 threads, one TMEM lane each) read the logits back, reduce
-//    per-row softmax statistics over the CTA's tokens and publish them; the last
-//    CTA to finish a slab merges all partial statistics with the look-ahead keys
-//    into lse and raises the slab's ready flag;
-//  * lag slabs later the same warps re-read the slab's logits from TMEM (not
-//    HBM), subtract lse, take the max over the G heads of each look-ahead step
-//    and fold it into a per-token running max kept in shared memory; the TMEM
-//    slot is then released to the MMA warp.
-// K is therefore read exactly once from HBM and the contraction runs once.
+// resident).  Every CTA owns one fixed range of prompt tokens (multiples of 32)
+// in every (layer, KV head) slab, so the max over heads and layers of a token
+// stays inside one CTA: no atomics on the data path, and importance is written
+// once.  Warp roles:
+//  * warp 0 (TMA): streams the CTA's K rows slab after slab (32-row x 128-byte
+//    boxes, 128B swizzle) through a ring of shared-memory stages, and the slab's
+//    query rows (a pre-swizzled image built by tc_prep_kernel) with one bulk copy;
+//  * warp 1 (MMA): tcgen05.mma, M = 128 tokens, N = 32 query rows (N*G padded),
+//    K = 16 per instruction, bf16 in, fp32 accumulate in TMEM; each slab has a
+//    TMEM slot holding all of the CTA's logits of that slab;
+//  * warps 2-9 (epilogue, two groups of four warps that split a slab's tiles,
+//    one TMEM lane per thread): per-row softmax statistics (max, sum of exp)
+//    over the CTA's tokens; `lag` slabs later the logits are read again from
+//    TMEM (not HBM), lse is subtracted, the max over the G heads of each
+//    look-ahead step is folded into a per-token running max in shared memory,
+//    and the TMEM slot goes back to the MMA warp;
+//  * warp 10 (publish): writes the CTA's statistics of each slab to global
+//    memory and bumps the slab's counter (no fence: each entry is a single
+//    64-bit store and a published entry always has z >= 1, so readers can tell
+//    published entries from the zeroed ones);
+//  * warps 11-14 (merge): CTA c merges slabs s = c, c + P, ...: once the counter
+//    shows every CTA's statistics it reads them (re-reading any entry still 0),
+//    adds the look-ahead keys and publishes lse as (value, tag) 64-bit entries;
+//  * warp 15 (fetch): waits until a slab's lse entries are all tagged and copies
+//    them into a shared-memory ring for the epilogue.
+// K is read exactly once from HBM and the contraction runs once.
 //
-// Every wait is bounded (mbarrier phases, the cross-CTA ready flags): on
-// timeout the kernel records SP_ETIMEOUT in the workspace header, all roles
-// stop, in-flight copies and MMAs are waited for (again bounded) and TMEM is
-// freed before the CTA exits.
+// Every wait is bounded: on timeout the kernel records SP_ETIMEOUT in the
+// workspace header, all roles stop, in-flight copies and MMAs are waited for
+// (again bounded) and TMEM is freed before the CTA exits.
 #include "sp_common.cuh"
 
 #include <cuda.h>
@@ -44,14 +49,19 @@
 namespace sp {
 namespace {
 
-constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue (128 threads)
+constexpr int kThreads = 512;        // 16 warps
+constexpr int kEpiBase = 64;         // warps 2-9: epilogue
+constexpr int kPubWarp = 10;
+constexpr int kMergeBase = 352;      // warps 11-14: merge
+constexpr int kFetchWarp = 15;
 constexpr int kTileRows = 128;       // tokens per MMA tile (MMA M)
 constexpr int kBoxRows = 32;         // rows per TMA box
 constexpr int kUnit = 32;            // token-range granularity
 constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 8;         // tiles per CTA per slab
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 16;
+constexpr int kRing = 4;             // entries of the statistics and lse rings
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
 
@@ -64,14 +74,13 @@ struct TcParams {
     int64_t T;          // rows per slab in K (= M for one prompt)
     float scale, scale_log2e;
     // shared-memory carve (byte offsets from the 1024-aligned base)
-    int off_q, off_s, off_acc, off_lse, off_bar, smem_bytes;
+    int off_q, off_s, off_acc, off_x, off_stats, off_lse, off_bar, smem_bytes;
     // workspace
-    const uint8_t* qimg;    // [S][kRP * d] bf16, 128B-swizzled image of the slab's query rows
-    const float2* la;       // [S][kRP] softmax statistics of the look-ahead keys
-    float2* partials;       // [S][P][kRP]
-    float* lse;             // [S][kRP]
-    unsigned* cnt;          // [S] CTAs done with a slab's statistics
-    unsigned* ready;        // [S] lse published
+    const uint8_t* qimg;            // [S][kRP * d] bf16, 128B-swizzled image of the slab's query rows
+    const float2* la;               // [S][kRP] softmax statistics of the look-ahead keys
+    unsigned long long* partials;   // [S][kRP][P] (m, z) as 64-bit words; 0 = not yet published
+    unsigned long long* lse;        // [S][kRP] (lse bits, tag 1); 0 = not yet published
+    unsigned* cnt;                  // [S] CTAs that published a slab's statistics
     WsHeader* hdr;
     float* importance;
 };
@@ -133,6 +142,40 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
     }
 }
 
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_cg64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.global.cg.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_relaxed(unsigned* p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+    return (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+}
+
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+    return make_float2(__uint_as_float((unsigned)(v & 0xffffffffu)), __uint_as_float((unsigned)(v >> 32)));
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -149,7 +192,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barriers: 1 and 2 = the two epilogue groups, 3 = whole epilogue, 4 = merge warps.
+__device__ __forceinline__ void group_sync(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+__device__ __forceinline__ void merge_sync() { asm volatile("bar.sync 4, 128;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row groups 1024 bytes apart.
@@ -203,16 +249,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Merge softmax statistics (m2, z2) into (m, z) (natural-log domain).
@@ -285,11 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     const int len = (int)(t_end - t_begin);
     const int n_tiles = (len + kTileRows - 1) / kTileRows;
 
-    uint8_t* k_stage = smem;                                   // [stages][kStageBytes]
-    uint8_t* q_buf = smem + p.off_q;                           // [2][kQBytes]
-    float* S = reinterpret_cast<float*>(smem + p.off_s);       // [kRP][4][33]
-    float* acc = reinterpret_cast<float*>(smem + p.off_acc);   // [n_tiles_max][N][128]
-    float* lse_s = reinterpret_cast<float*>(smem + p.off_lse); // [kRP]
+    uint8_t* k_stage = smem;                                       // [stages][kStageBytes]
+    uint8_t* q_buf = smem + p.off_q;                               // [2][kQBytes]
+    float* Sbuf = reinterpret_cast<float*>(smem + p.off_s);        // [2 groups][kRP][4][33]
+    float* acc = reinterpret_cast<float*>(smem + p.off_acc);       // [n_tiles_max][N][128]
+    float2* xchg = reinterpret_cast<float2*>(smem + p.off_x);      // [kRP] group 1 -> group 0
+    float2* stats = reinterpret_cast<float2*>(smem + p.off_stats); // [kRing][kRP]
+    float* lse_ring = reinterpret_cast<float*>(smem + p.off_lse);  // [kRing][kRP]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* k_full = bars;
     uint64_t* k_empty = bars + p.stages;
@@ -297,10 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     uint64_t* q_empty = q_full + 2;
     uint64_t* slot_full = q_empty + 2;
     uint64_t* slot_empty = slot_full + kMaxSlots;
-    uint64_t* final_bar = slot_empty + kMaxSlots;
+    uint64_t* stats_full = slot_empty + kMaxSlots;
+    uint64_t* stats_empty = stats_full + kRing;
+    uint64_t* lse_full = stats_empty + kRing;
+    uint64_t* lse_empty = lse_full + kRing;
+    uint64_t* final_bar = lse_empty + kRing;
     volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(final_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
-    volatile int* last_flag = abort_flag + 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -315,9 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             mbar_init(smem_u32(&slot_full[i]), 1);
             mbar_init(smem_u32(&slot_empty[i]), 1);
         }
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(smem_u32(&stats_full[i]), 1);
+            mbar_init(smem_u32(&stats_empty[i]), 1);
+            mbar_init(smem_u32(&lse_full[i]), 1);
+            mbar_init(smem_u32(&lse_empty[i]), 1);
+        }
         mbar_init(smem_u32(final_bar), 1);
         *abort_flag = 0;
-        *last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -348,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 const int64_t row0 = (int64_t)s * p.T + t_begin;
                 for (int t = 0; t < n_tiles; ++t, ++it) {
                     const int st = it % p.stages;
-                    if (it >= p.stages) ok = mbar_wait(smem_u32(&k_empty[st]), ((it / p.stages) - 1) & 1, abort_flag, p.hdr, 2);
+                    if (it >= p.stages)
+                        ok = mbar_wait(smem_u32(&k_empty[st]), ((it / p.stages) - 1) & 1, abort_flag, p.hdr, 2);
                     if (!ok) break;
                     const int rows = min(kTileRows, len - t * kTileRows);
                     const int nbox = (rows + kBoxRows - 1) / kBoxRows;
@@ -409,30 +456,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 if (global_ns() - t0 > kTimeoutNs) break;
         }
         __syncwarp();
-    } else {
+    } else if (warp < kPubWarp) {
         // ------------------------------ epilogue ------------------------------
-        const int e = threadIdx.x - 64;                // 0..127
+        const int e = threadIdx.x - kEpiBase;          // 0..255
+        const int grp = e >> 7, ge = e & 127;          // group 0 takes even tiles, group 1 odd tiles
         const int quad = warp & 3;                     // TMEM lane quadrant of this warp
         const int tok = quad * 32 + lane;              // token row inside a tile
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        const int r_e = e >> 2, part = e & 3;          // reduction role: row r_e, quarter `part`
+        const int r_e = ge >> 2, part = ge & 3;        // reduction role: row r_e, quarter `part`
+        float* S = Sbuf + grp * (kRP * 4 * 33);
         bool ok = true;
         for (int step = 0; step < p.S + p.lag && ok; ++step) {
             // ---- statistics of slab `step` ----
             if (step < p.S) {
-                const int s = step, slot = s % p.NS;
-                if (e == 0) mbar_wait(smem_u32(&slot_full[slot]), (s / p.NS) & 1, abort_flag, p.hdr, 6);
+                const int s = step, slot = s % p.NS, q = s % kRing;
+                if (e == 0) {
+                    mbar_wait(smem_u32(&slot_full[slot]), (s / p.NS) & 1, abort_flag, p.hdr, 6);
+                    if (s >= kRing) mbar_wait(smem_u32(&stats_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 7);
+                }
                 epi_sync();
                 if (*abort_flag) { ok = false; break; }
                 tc_fence_after();
                 float m_run = -INFINITY, z_run = 0.f;
-                for (int t = 0; t < n_tiles; ++t) {
+                for (int t = grp; t < n_tiles; t += 2) {
                     float x[32];
                     tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
                     const bool valid = t * kTileRows + tok < len;
 #pragma unroll
                     for (int r = 0; r < kRP; ++r) S[(r * 4 + quad) * 33 + lane] = valid ? x[r] : -INFINITY;
-                    epi_sync();
+                    group_sync(grp);
                     const float* row = S + (r_e * 4 + part) * 33;
                     float mx = -INFINITY;
 #pragma unroll
@@ -441,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     if (mx != -INFINITY) {
                         const float off = mx * p.scale_log2e;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) z += exp2f(fmaf(row[i], p.scale_log2e, -off));
+                        for (int i = 0; i < 32; ++i) z += ex2_approx(fmaf(row[i], p.scale_log2e, -off));
                     }
                     float m = mx == -INFINITY ? -INFINITY : mx * p.scale;
 #pragma unroll
@@ -451,62 +503,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                         merge(m, z, m2, z2);
                     }
                     merge(m_run, z_run, m, z);
-                    epi_sync();
+                    group_sync(grp);
                 }
-                if (part == 0) p.partials[((size_t)s * p.P + c) * kRP + r_e] = make_float2(m_run, z_run);
-                __threadfence();
+                if (grp == 1 && part == 0) xchg[r_e] = make_float2(m_run, z_run);
                 epi_sync();
-                if (e == 0) {
-                    const unsigned prev = atomicAdd(&p.cnt[s], 1u);
-                    *last_flag = (prev == (unsigned)p.P - 1u) ? 1 : 0;
+                if (grp == 0 && part == 0) {
+                    const float2 o = xchg[r_e];
+                    merge(m_run, z_run, o.x, o.y);
+                    stats[q * kRP + r_e] = make_float2(m_run, z_run);
                 }
                 epi_sync();
-                if (*last_flag) {
-                    // the last CTA to finish slab s merges every CTA's statistics into lse
-                    __threadfence();
-                    float m = -INFINITY, z = 0.f;
-                    for (int cc = part; cc < p.P; cc += 4) {
-                        const float2 v = __ldcg(&p.partials[((size_t)s * p.P + cc) * kRP + r_e]);
-                        merge(m, z, v.x, v.y);
-                    }
-#pragma unroll
-                    for (int o = 1; o <= 2; o <<= 1) {
-                        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-                        const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
-                        merge(m, z, m2, z2);
-                    }
-                    if (part == 0) {
-                        const float2 v = __ldcg(&p.la[(size_t)s * kRP + r_e]);
-                        merge(m, z, v.x, v.y);
-                        p.lse[(size_t)s * kRP + r_e] = m + __logf(z);
-                    }
-                    __threadfence();
-                    epi_sync();
-                    if (e == 0) st_release(&p.ready[s], 1u);
-                }
+                if (e == 0) mbar_arrive(smem_u32(&stats_full[q]));
             }
             // ---- normalise + max of slab `step - lag` ----
             if (step >= p.lag) {
-                const int s = step - p.lag, slot = s % p.NS;
-                if (e == 0) {
-                    const unsigned long long t0 = global_ns();
-                    unsigned i = 0;
-                    while (ld_acquire(&p.ready[s]) == 0u) {
-                        if (*abort_flag) break;
-                        if ((++i & 15u) == 0 && global_ns() - t0 > kTimeoutNs) {
-                            record_error(p.hdr, SP_ETIMEOUT, 100 + (s & 0xFF));
-                            *abort_flag = 1;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                }
+                const int s = step - p.lag, slot = s % p.NS, q = s % kRing;
+                if (e == 0) mbar_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8);
                 epi_sync();
                 if (*abort_flag) { ok = false; break; }
-                if (e < kRP) lse_s[e] = __ldcg(&p.lse[(size_t)s * kRP + e]);
-                epi_sync();
+                const float* lse_s = lse_ring + q * kRP;
                 tc_fence_after();
-                for (int t = 0; t < n_tiles; ++t) {
+                for (int t = grp; t < n_tiles; t += 2) {
                     float x[32];
                     tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
                     float* a = acc + (size_t)t * p.N * kTileRows + tok;
@@ -523,13 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 }
                 tc_fence_before();
                 epi_sync();
-                if (e == 0) mbar_arrive(smem_u32(&slot_empty[slot]));
+                if (e == 0) {
+                    mbar_arrive(smem_u32(&slot_empty[slot]));
+                    mbar_arrive(smem_u32(&lse_empty[q]));
+                }
             }
         }
         if (ok) {
             // importance of this CTA's tokens: (1/N) sum_j exp(max_{l,h}(s - lse))
             const float inv_n = 1.0f / (float)p.N;
-            for (int t = 0; t < n_tiles; ++t) {
+            for (int t = grp; t < n_tiles; t += 2) {
                 const int i = t * kTileRows + tok;
                 if (i < len) {
                     const float* a = acc + (size_t)t * p.N * kTileRows + tok;
@@ -538,6 +558,114 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     p.importance[t_begin + i] = sum * inv_n;
                 }
             }
+        }
+    } else if (warp == kPubWarp) {
+        // ------------------------------ publish ------------------------------
+        for (int s = 0; s < p.S; ++s) {
+            const int q = s % kRing;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(smem_u32(&stats_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 9);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            __syncwarp();
+            if (!ok) break;
+            const float2 v = stats[q * kRP + lane];
+            st64(&p.partials[((size_t)s * kRP + lane) * p.P + c], pack2(v.x, v.y));
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&stats_empty[q]));
+                red_add_relaxed(&p.cnt[s], 1u);
+            }
+        }
+    } else if (warp < kFetchWarp) {
+        // ------------------------------ merge ------------------------------
+        const int mi = threadIdx.x - kMergeBase;       // 0..127
+        const int r = mi >> 2, part = mi & 3;
+        for (int s = c; s < p.S; s += p.P) {
+            if (mi == 0) {
+                const unsigned long long t0 = global_ns();
+                for (unsigned i = 0; ld_relaxed(&p.cnt[s]) < (unsigned)p.P; ++i) {
+                    if (*abort_flag) break;
+                    if ((i & 15u) == 15u && global_ns() - t0 > kTimeoutNs) {
+                        record_error(p.hdr, SP_ETIMEOUT, 12);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            merge_sync();
+            if (*abort_flag) break;
+            const unsigned long long* src = p.partials + ((size_t)s * kRP + r) * p.P;
+            float m = -INFINITY, z = 0.f;
+            bool ok = true;
+            for (int base = part; base < p.P && ok; base += 64) {
+                unsigned long long v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int cc = base + 4 * k;
+                    v[k] = cc < p.P ? ld_cg64(src + cc) : 0ull;
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int cc = base + 4 * k;
+                    if (cc >= p.P) continue;
+                    // an entry whose store is not visible yet reads as 0: read it again
+                    const unsigned long long t0 = global_ns();
+                    while ((v[k] >> 32) == 0ull) {
+                        if (*abort_flag || global_ns() - t0 > kTimeoutNs) { ok = false; break; }
+                        v[k] = ld_cg64(src + cc);
+                    }
+                    const float2 f = unpack2(v[k]);
+                    merge(m, z, f.x, f.y);
+                }
+            }
+            if (!ok) {
+                record_error(p.hdr, SP_ETIMEOUT, 13);
+                *abort_flag = 1;
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+                merge(m, z, m2, z2);
+            }
+            if (part == 0) {
+                const float2 v = __ldcg(&p.la[(size_t)s * kRP + r]);
+                merge(m, z, v.x, v.y);
+                const float lse = m + __logf(z);
+                st64(&p.lse[(size_t)s * kRP + r], (unsigned long long)__float_as_uint(lse) | (1ull << 32));
+            }
+            merge_sync();
+        }
+    } else {
+        // ------------------------------ fetch ------------------------------
+        for (int s = 0; s < p.S; ++s) {
+            const int q = s % kRing;
+            bool ok = true;
+            if (lane == 0 && s >= kRing) ok = mbar_wait(smem_u32(&lse_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 10);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            __syncwarp();
+            if (!ok) break;
+            const unsigned long long* src = p.lse + (size_t)s * kRP + lane;
+            unsigned long long v = ld_cg64(src);
+            const unsigned long long t0 = global_ns();
+            while (!__all_sync(0xffffffffu, (v >> 32) == 1ull)) {
+                if (*abort_flag) { ok = false; break; }
+                if (global_ns() - t0 > kTimeoutNs) {
+                    if (lane == 0) {
+                        record_error(p.hdr, SP_ETIMEOUT, 11);
+                        *abort_flag = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
+                v = ld_cg64(src);
+            }
+            if (!ok) break;
+            lse_ring[q * kRP + lane] = __uint_as_float((unsigned)(v & 0xffffffffu));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&lse_full[q]));
         }
     }
     tc_fence_before();
@@ -555,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
 struct Plan {
     TcParams p;
-    size_t off_qimg, off_la, off_partials, off_lse, off_cnt, off_ready, total;
+    size_t off_qimg, off_la, off_partials, off_lse, off_cnt, total;
 };
 
 int sm_count_or(int fallback) {
@@ -594,26 +722,38 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     p.slot_cols = p.n_tiles_max * kRP;
     p.NS = std::min(kMaxSlots, 512 / p.slot_cols);
     if (p.NS < 2) return false;
-    p.lag = p.NS - 1;
+    // slabs held between their statistics and their normalise pass; one more
+    // slot lets the MMA warp run a slab ahead when there are enough slots
+    p.lag = p.NS >= 4 ? p.NS - 2 : p.NS - 1;
     int cols = 32;
     while (cols < p.NS * p.slot_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.scale = 1.0f / sqrtf((float)q.d);
     p.scale_log2e = p.scale * 1.4426950408889634f;
     const int stage_bytes = kTileRows * q.d * 2;
-    p.stages = q.d == 128 ? 4 : 8;
+    const int fixed = 2 * kRP * q.d * 2                      // query images
+                      + 2 * kRP * 4 * 33 * 4                  // reduction buffers
+                      + p.n_tiles_max * p.N * kTileRows * 4   // running max
+                      + kRP * 8 + kRing * kRP * 8 + kRing * kRP * 4 + 16
+                      + (2 * 8 + 4 + 2 * kMaxSlots + 4 * kRing + 1) * 8 + 16 + 1024;
+    p.stages = std::min(q.d == 128 ? 4 : 8, (kSmemBudget - fixed) / stage_bytes);
+    if (p.stages < 2) return false;
     int off = p.stages * stage_bytes;
     p.off_q = off;
     off += 2 * kRP * q.d * 2;
     p.off_s = off;
-    off += kRP * 4 * 33 * 4;
+    off += 2 * kRP * 4 * 33 * 4;
     p.off_acc = off;
     off += p.n_tiles_max * p.N * kTileRows * 4;
+    p.off_x = off;
+    off += kRP * 8;
+    p.off_stats = off;
+    off += kRing * kRP * 8;
     p.off_lse = off;
-    off += kRP * 4;
+    off += kRing * kRP * 4;
     off = (off + 15) & ~15;
     p.off_bar = off;
-    off += (2 * p.stages + 4 + 2 * kMaxSlots + 1) * 8 + 16;
+    off += (2 * p.stages + 4 + 2 * kMaxSlots + 4 * kRing + 1) * 8 + 16;
     p.smem_bytes = off + 1024;                    // slack for 1024-byte alignment
     if (p.smem_bytes > kSmemBudget) return false;
     // workspace (after the 256-byte header)
@@ -621,10 +761,9 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     const size_t S = (size_t)p.S;
     out.off_qimg = cv.take(S * kRP * q.d * 2);
     out.off_la = cv.take(S * kRP * sizeof(float2));
-    out.off_partials = cv.take(S * kMaxCtas * kRP * sizeof(float2));
-    out.off_lse = cv.take(S * kRP * sizeof(float));
-    out.off_cnt = cv.take(S * sizeof(unsigned));
-    out.off_ready = cv.take(S * sizeof(unsigned));
+    out.off_cnt = cv.take(S * sizeof(unsigned));          // cnt, lse, partials: zeroed per call
+    out.off_lse = cv.take(S * kRP * 8);
+    out.off_partials = cv.take(S * kRP * (size_t)kMaxCtas * 8);
     out.total = cv.off;
     return true;
 }
@@ -703,10 +842,9 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     p.hdr = reinterpret_cast<WsHeader*>(w);
     p.qimg = w + plan.off_qimg;
     p.la = reinterpret_cast<const float2*>(w + plan.off_la);
-    p.partials = reinterpret_cast<float2*>(w + plan.off_partials);
-    p.lse = reinterpret_cast<float*>(w + plan.off_lse);
+    p.partials = reinterpret_cast<unsigned long long*>(w + plan.off_partials);
+    p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
     p.cnt = reinterpret_cast<unsigned*>(w + plan.off_cnt);
-    p.ready = reinterpret_cast<unsigned*>(w + plan.off_ready);
     p.importance = q.importance;
 
     // K viewed as a 2D tensor of L*H_kv*T rows by d bf16 columns; 32-row x 64-column boxes.
@@ -723,8 +861,11 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
         return SP_ECUDA;
     }
 
+    // zero the header, the counters, the tagged lse entries and the partial
+    // statistics this launch uses ([S][kRP][P] words)
     SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
-    SP_CUDA_TRY(cudaMemsetAsync(w + plan.off_cnt, 0, plan.total - plan.off_cnt, st));
+    SP_CUDA_TRY(cudaMemsetAsync(w + plan.off_cnt, 0,
+                                plan.off_partials - plan.off_cnt + (size_t)p.S * kRP * p.P * 8, st));
     tc_prep_kernel<<<p.S, 256, 0, st>>>(p, static_cast<const __nv_bfloat16*>(q.Q),
                                         static_cast<const __nv_bfloat16*>(q.Kla), w + plan.off_qimg,
                                         reinterpret_cast<float2*>(w + plan.off_la));
