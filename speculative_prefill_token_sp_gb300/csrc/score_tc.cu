@@ -61,7 +61,7 @@ constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 8;         // tiles per CTA per slab
 constexpr int kMaxSlots = 16;
-constexpr int kRing = 4;             // entries of the statistics and lse rings
+constexpr int kRing = 8;             // entries of the statistics and lse rings
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
 
@@ -72,7 +72,9 @@ struct TcParams {
     int U;              // 32-token units of the prompt
     int n_tiles_max, slot_cols, NS, lag, tmem_cols, stages;
     int64_t T;          // rows per slab in K (= M for one prompt)
+    int pf_bytes;       // bytes of K each CTA keeps requested into L2 ahead of its shared-memory loads
     float scale, scale_log2e;
+    const uint8_t* kbase;   // K_prompt
     // shared-memory carve (byte offsets from the 1024-aligned base)
     int off_q, off_s, off_acc, off_x, off_stats, off_lse, off_bar, smem_bytes;
     // workspace
@@ -158,8 +160,10 @@ __device__ __forceinline__ void st64(unsigned long long* p, unsigned long long v
     asm volatile("st.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ void red_add_relaxed(unsigned* p, unsigned v) {
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Release: the warp's earlier stores (ordered before this by __syncwarp) become
+// visible no later than the increment.
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long pack2(float a, float b) {
@@ -181,6 +185,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -323,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
     uint8_t* k_stage = smem;                                       // [stages][kStageBytes]
     uint8_t* q_buf = smem + p.off_q;                               // [2][kQBytes]
-    float* Sbuf = reinterpret_cast<float*>(smem + p.off_s);        // [2 groups][kRP][4][33]
-    float* acc = reinterpret_cast<float*>(smem + p.off_acc);       // [n_tiles_max][N][128]
+    float* Sbuf = reinterpret_cast<float*>(smem + p.off_s);        // [2 groups][2 buffers][kRP][4][33]
+    float* acc = reinterpret_cast<float*>(smem + p.off_acc);       // [2 groups][n_tiles_max][N][128]
     float2* xchg = reinterpret_cast<float2*>(smem + p.off_x);      // [kRP] group 1 -> group 0
     float2* stats = reinterpret_cast<float2*>(smem + p.off_stats); // [kRing][kRP]
     float* lse_ring = reinterpret_cast<float*>(smem + p.off_lse);  // [kRing][kRP]
@@ -340,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     uint64_t* lse_full = stats_empty + kRing;
     uint64_t* lse_empty = lse_full + kRing;
     uint64_t* final_bar = lse_empty + kRing;
-    volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(final_bar + 1);
+    uint64_t* merge_go = final_bar + 1;
+    volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(merge_go + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
 
     if (threadIdx.x == 0) {
@@ -363,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             mbar_init(smem_u32(&lse_empty[i]), 1);
         }
         mbar_init(smem_u32(final_bar), 1);
+        mbar_init(smem_u32(merge_go), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -373,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     // running max of (s - lse) over (layer, head), per token and look-ahead step
-    for (int i = threadIdx.x; i < p.n_tiles_max * p.N * kTileRows; i += kThreads) acc[i] = -INFINITY;
+    for (int i = threadIdx.x; i < 2 * p.n_tiles_max * p.N * kTileRows; i += kThreads) acc[i] = -INFINITY;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -384,7 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         if (lane == 0) {
             int it = 0;
             bool ok = true;
+            // This CTA's rows of one slab are one contiguous byte range: keep the
+            // next `pf` slabs' ranges requested into L2 so that enough bytes are in
+            // flight per SM to cover the loaded memory latency; the shared-memory
+            // loads then hit L2.
+            const uint32_t slab_bytes = (uint32_t)len * D * 2;
+            const int pf = max(1, min(16, (int)((p.pf_bytes + slab_bytes - 1) / slab_bytes)));
+            for (int s = 0; s < min(pf, p.S); ++s)
+                prefetch_l2(p.kbase + ((size_t)s * p.T + t_begin) * D * 2, slab_bytes);
             for (int s = 0; s < p.S && ok; ++s) {
+                if (s + pf < p.S) prefetch_l2(p.kbase + ((size_t)(s + pf) * p.T + t_begin) * D * 2, slab_bytes);
                 const int qb = s & 1;
                 if (s >= 2) ok = mbar_wait(smem_u32(&q_empty[qb]), ((s >> 1) - 1) & 1, abort_flag, p.hdr, 1);
                 if (!ok) break;
@@ -458,42 +477,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         __syncwarp();
     } else if (warp < kPubWarp) {
         // ------------------------------ epilogue ------------------------------
+        // Two independent groups of four warps: group g handles slabs g, g + 2, ...
+        // with its own barrier, so one group's waits overlap the other's work.
         const int e = threadIdx.x - kEpiBase;          // 0..255
-        const int grp = e >> 7, ge = e & 127;          // group 0 takes even tiles, group 1 odd tiles
+        const int grp = e >> 7, ge = e & 127;
         const int quad = warp & 3;                     // TMEM lane quadrant of this warp
         const int tok = quad * 32 + lane;              // token row inside a tile
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
         const int r_e = ge >> 2, part = ge & 3;        // reduction role: row r_e, quarter `part`
-        float* S = Sbuf + grp * (kRP * 4 * 33);
+        float* S2 = Sbuf + grp * (2 * kRP * 4 * 33);   // two buffers per group, alternating by tile
+        float* acc_g = acc + (size_t)grp * p.n_tiles_max * p.N * kTileRows;
+        int tb = 0;
         bool ok = true;
-        for (int step = 0; step < p.S + p.lag && ok; ++step) {
-            // ---- statistics of slab `step` ----
-            if (step < p.S) {
-                const int s = step, slot = s % p.NS, q = s % kRing;
-                if (e == 0) {
+        const int n_own = (p.S - grp + 1) / 2;         // slabs of this group
+        for (int i = 0; i < n_own + p.lag && ok; ++i) {
+            // ---- statistics of this group's i-th slab ----
+            if (i < n_own) {
+                const int s = 2 * i + grp, slot = s % p.NS, q = s % kRing;
+                if (ge == 0) {
                     mbar_wait(smem_u32(&slot_full[slot]), (s / p.NS) & 1, abort_flag, p.hdr, 6);
                     if (s >= kRing) mbar_wait(smem_u32(&stats_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 7);
                 }
-                epi_sync();
+                group_sync(grp);
                 if (*abort_flag) { ok = false; break; }
                 tc_fence_after();
                 float m_run = -INFINITY, z_run = 0.f;
-                for (int t = grp; t < n_tiles; t += 2) {
+                for (int t = 0; t < n_tiles; ++t) {
                     float x[32];
                     tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
                     const bool valid = t * kTileRows + tok < len;
+                    // The buffer written here was last read two tiles ago; every thread
+                    // has passed this group's barrier of the tile in between since.
+                    float* S = S2 + tb * (kRP * 4 * 33);
+                    tb ^= 1;
 #pragma unroll
                     for (int r = 0; r < kRP; ++r) S[(r * 4 + quad) * 33 + lane] = valid ? x[r] : -INFINITY;
                     group_sync(grp);
                     const float* row = S + (r_e * 4 + part) * 33;
-                    float mx = -INFINITY;
+                    float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, row[i]);
+                    for (int k = 0; k < 32; ++k) v[k] = row[k];
+                    float mq[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+                    for (int k = 4; k < 32; ++k) mq[k & 3] = fmaxf(mq[k & 3], v[k]);
+                    const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
                     float z = 0.f;
                     if (mx != -INFINITY) {
                         const float off = mx * p.scale_log2e;
+                        float zq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) z += ex2_approx(fmaf(row[i], p.scale_log2e, -off));
+                        for (int k = 0; k < 32; ++k) zq[k & 3] += ex2_approx(fmaf(v[k], p.scale_log2e, -off));
+                        z = (zq[0] + zq[1]) + (zq[2] + zq[3]);
                     }
                     float m = mx == -INFINITY ? -INFINITY : mx * p.scale;
 #pragma unroll
@@ -503,59 +537,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                         merge(m, z, m2, z2);
                     }
                     merge(m_run, z_run, m, z);
-                    group_sync(grp);
                 }
-                if (grp == 1 && part == 0) xchg[r_e] = make_float2(m_run, z_run);
-                epi_sync();
-                if (grp == 0 && part == 0) {
-                    const float2 o = xchg[r_e];
-                    merge(m_run, z_run, o.x, o.y);
-                    stats[q * kRP + r_e] = make_float2(m_run, z_run);
-                }
-                epi_sync();
-                if (e == 0) mbar_arrive(smem_u32(&stats_full[q]));
+                if (part == 0) stats[q * kRP + r_e] = make_float2(m_run, z_run);
+                group_sync(grp);
+                if (ge == 0) mbar_arrive(smem_u32(&stats_full[q]));
             }
-            // ---- normalise + max of slab `step - lag` ----
-            if (step >= p.lag) {
-                const int s = step - p.lag, slot = s % p.NS, q = s % kRing;
-                if (e == 0) mbar_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8);
-                epi_sync();
+            // ---- normalise + max of this group's (i - lag)-th slab ----
+            if (i >= p.lag) {
+                const int s = 2 * (i - p.lag) + grp, slot = s % p.NS, q = s % kRing;
+                if (ge == 0) mbar_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8);
+                group_sync(grp);
                 if (*abort_flag) { ok = false; break; }
-                const float* lse_s = lse_ring + q * kRP;
+                float lr[kRP];
+#pragma unroll
+                for (int r = 0; r < kRP; ++r) lr[r] = lse_ring[q * kRP + r];
                 tc_fence_after();
-                for (int t = grp; t < n_tiles; t += 2) {
+                for (int t = 0; t < n_tiles; ++t) {
                     float x[32];
                     tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
-                    float* a = acc + (size_t)t * p.N * kTileRows + tok;
+                    float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
 #pragma unroll
                     for (int j = 0; j < kRP / G; ++j) {
                         if (j < p.N) {
                             float y = -INFINITY;
 #pragma unroll
                             for (int hh = 0; hh < G; ++hh)
-                                y = fmaxf(y, fmaf(x[j * G + hh], p.scale, -lse_s[j * G + hh]));
+                                y = fmaxf(y, fmaf(x[j * G + hh], p.scale, -lr[j * G + hh]));
                             a[j * kTileRows] = fmaxf(a[j * kTileRows], y);
                         }
                     }
                 }
                 tc_fence_before();
-                epi_sync();
-                if (e == 0) {
+                group_sync(grp);
+                if (ge == 0) {
                     mbar_arrive(smem_u32(&slot_empty[slot]));
                     mbar_arrive(smem_u32(&lse_empty[q]));
                 }
             }
         }
-        if (ok) {
+        epi_sync();                                    // both groups' running maxima are complete
+        if (!*abort_flag) {
             // importance of this CTA's tokens: (1/N) sum_j exp(max_{l,h}(s - lse))
             const float inv_n = 1.0f / (float)p.N;
+            const size_t half = (size_t)p.n_tiles_max * p.N * kTileRows;
             for (int t = grp; t < n_tiles; t += 2) {
-                const int i = t * kTileRows + tok;
-                if (i < len) {
+                const int k = t * kTileRows + tok;
+                if (k < len) {
                     const float* a = acc + (size_t)t * p.N * kTileRows + tok;
                     float sum = 0.f;
-                    for (int j = 0; j < p.N; ++j) sum += expf(a[j * kTileRows]);
-                    p.importance[t_begin + i] = sum * inv_n;
+                    for (int j = 0; j < p.N; ++j) sum += expf(fmaxf(a[j * kTileRows], a[half + j * kTileRows]));
+                    p.importance[t_begin + k] = sum * inv_n;
                 }
             }
         }
@@ -573,51 +604,59 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(&stats_empty[q]));
-                red_add_relaxed(&p.cnt[s], 1u);
+                // this CTA merges slab s: start reading the other CTAs' statistics now
+                if (s % p.P == c) mbar_arrive(smem_u32(merge_go));
             }
         }
     } else if (warp < kFetchWarp) {
         // ------------------------------ merge ------------------------------
+        // Slab s is merged by CTA s mod P, once this CTA has published its own
+        // statistics of s (the other CTAs are then a few microseconds from done):
+        // the entries are read until every CTA's is there.
         const int mi = threadIdx.x - kMergeBase;       // 0..127
         const int r = mi >> 2, part = mi & 3;
-        for (int s = c; s < p.S; s += p.P) {
-            if (mi == 0) {
-                const unsigned long long t0 = global_ns();
-                for (unsigned i = 0; ld_relaxed(&p.cnt[s]) < (unsigned)p.P; ++i) {
-                    if (*abort_flag) break;
-                    if ((i & 15u) == 15u && global_ns() - t0 > kTimeoutNs) {
-                        record_error(p.hdr, SP_ETIMEOUT, 12);
-                        *abort_flag = 1;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
+        for (int s = c, k_go = 0; s < p.S; s += p.P, ++k_go) {
+            if (mi == 0) mbar_wait(smem_u32(merge_go), k_go & 1, abort_flag, p.hdr, 12);
             merge_sync();
             if (*abort_flag) break;
             const unsigned long long* src = p.partials + ((size_t)s * kRP + r) * p.P;
             float m = -INFINITY, z = 0.f;
             bool ok = true;
-            for (int base = part; base < p.P && ok; base += 64) {
-                unsigned long long v[16];
+            for (int base = part; base < p.P && ok; base += 128) {
+                // all loads of the batch first (up to 32 in flight per thread)
+                unsigned long long v[32];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
+                for (int k = 0; k < 32; ++k) {
                     const int cc = base + 4 * k;
                     v[k] = cc < p.P ? ld_cg64(src + cc) : 0ull;
                 }
+                // an entry whose store is not visible yet reads as 0: read the missing
+                // ones again, all in flight together
+                const unsigned long long t0 = global_ns();
+                for (;;) {
+                    bool missing = false;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int cc = base + 4 * k;
-                    if (cc >= p.P) continue;
-                    // an entry whose store is not visible yet reads as 0: read it again
-                    const unsigned long long t0 = global_ns();
-                    while ((v[k] >> 32) == 0ull) {
-                        if (*abort_flag || global_ns() - t0 > kTimeoutNs) { ok = false; break; }
-                        v[k] = ld_cg64(src + cc);
-                    }
-                    const float2 f = unpack2(v[k]);
-                    merge(m, z, f.x, f.y);
+                    for (int k = 0; k < 32; ++k)
+                        if (base + 4 * k < p.P && (v[k] >> 32) == 0ull) missing = true;
+                    if (!missing) break;
+                    if (*abort_flag || global_ns() - t0 > kTimeoutNs) { ok = false; break; }
+                    __nanosleep(64);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        if (base + 4 * k < p.P && (v[k] >> 32) == 0ull) v[k] = ld_cg64(src + base + 4 * k);
                 }
+                float mb = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (base + 4 * k < p.P) mb = fmaxf(mb, unpack2(v[k]).x);
+                float zb = 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    if (base + 4 * k >= p.P) continue;
+                    const float2 f = unpack2(v[k]);
+                    zb += f.y * __expf(f.x - mb);
+                }
+                merge(m, z, mb, zb);
             }
             if (!ok) {
                 record_error(p.hdr, SP_ETIMEOUT, 13);
@@ -724,27 +763,31 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     if (p.NS < 2) return false;
     // slabs held between their statistics and their normalise pass; one more
     // slot lets the MMA warp run a slab ahead when there are enough slots
-    p.lag = p.NS >= 4 ? p.NS - 2 : p.NS - 1;
+    // Each epilogue group holds lag + 1 of its own slabs (every other slab) in
+    // TMEM; with enough slots one more group-step lets the MMA warp run ahead.
+    p.NS &= ~1;
+    p.lag = p.NS >= 8 ? p.NS / 2 - 2 : p.NS / 2 - 1;
     int cols = 32;
     while (cols < p.NS * p.slot_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.scale = 1.0f / sqrtf((float)q.d);
     p.scale_log2e = p.scale * 1.4426950408889634f;
+    p.pf_bytes = 192 * 1024;
     const int stage_bytes = kTileRows * q.d * 2;
     const int fixed = 2 * kRP * q.d * 2                      // query images
-                      + 2 * kRP * 4 * 33 * 4                  // reduction buffers
-                      + p.n_tiles_max * p.N * kTileRows * 4   // running max
+                      + 4 * kRP * 4 * 33 * 4                  // reduction buffers (2 groups x 2)
+                      + 2 * p.n_tiles_max * p.N * kTileRows * 4   // running max (one per group)
                       + kRP * 8 + kRing * kRP * 8 + kRing * kRP * 4 + 16
-                      + (2 * 8 + 4 + 2 * kMaxSlots + 4 * kRing + 1) * 8 + 16 + 1024;
-    p.stages = std::min(q.d == 128 ? 4 : 8, (kSmemBudget - fixed) / stage_bytes);
+                      + (2 * 8 + 4 + 2 * kMaxSlots + 4 * kRing + 2) * 8 + 16 + 1024;
+    p.stages = std::min(8, (kSmemBudget - fixed) / stage_bytes);
     if (p.stages < 2) return false;
     int off = p.stages * stage_bytes;
     p.off_q = off;
     off += 2 * kRP * q.d * 2;
     p.off_s = off;
-    off += 2 * kRP * 4 * 33 * 4;
+    off += 4 * kRP * 4 * 33 * 4;
     p.off_acc = off;
-    off += p.n_tiles_max * p.N * kTileRows * 4;
+    off += 2 * p.n_tiles_max * p.N * kTileRows * 4;
     p.off_x = off;
     off += kRP * 8;
     p.off_stats = off;
@@ -753,7 +796,7 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     off += kRing * kRP * 4;
     off = (off + 15) & ~15;
     p.off_bar = off;
-    off += (2 * p.stages + 4 + 2 * kMaxSlots + 4 * kRing + 1) * 8 + 16;
+    off += (2 * p.stages + 4 + 2 * kMaxSlots + 4 * kRing + 2) * 8 + 16;
     p.smem_bytes = off + 1024;                    // slack for 1024-byte alignment
     if (p.smem_bytes > kSmemBudget) return false;
     // workspace (after the 256-byte header)
@@ -846,6 +889,7 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
     p.cnt = reinterpret_cast<unsigned*>(w + plan.off_cnt);
     p.importance = q.importance;
+    p.kbase = static_cast<const uint8_t*>(q.K);
 
     // K viewed as a 2D tensor of L*H_kv*T rows by d bf16 columns; 32-row x 64-column boxes.
     CUtensorMap map;
