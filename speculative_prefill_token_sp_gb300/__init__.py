@@ -227,8 +227,14 @@ def _workspace(nbytes: int, device, ws=None):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
-def score(Q_la, K_prompt, K_la, *, importance=None, ws=None, stream=None):
-    """Importance [M] (fp32) of one prompt: Q_la [N,L,H,d], K_prompt [L,H_kv,M,d], K_la [L,H_kv,N,d]."""
+def _check_device(ws, stream, check):
+    if check:
+        _check(sp_workspace_status(ws, stream))
+
+
+def score(Q_la, K_prompt, K_la, *, importance=None, ws=None, stream=None, check=False):
+    """Importance [M] (fp32) of one prompt: Q_la [N,L,H,d], K_prompt [L,H_kv,M,d], K_la [L,H_kv,N,d].
+    check=True synchronises and raises if a kernel recorded a run-time error."""
     import torch
     N, L, H, d = Q_la.shape
     _, H_kv, M, _ = K_prompt.shape
@@ -238,10 +244,11 @@ def score(Q_la, K_prompt, K_la, *, importance=None, ws=None, stream=None):
     need = sp_score_workspace_size(L, H, H_kv, d, M, N, dt)
     ws = _workspace(need, K_prompt.device, ws)
     _check(sp_score(Q_la, K_prompt, K_la, L, H, H_kv, d, M, N, dt, importance, ws, ws.numel(), stream))
+    _check_device(ws, stream, check)
     return importance
 
 
-def score_varlen(Q_la, K_prompt, K_la, cu_M, *, importance=None, ws=None, stream=None):
+def score_varlen(Q_la, K_prompt, K_la, cu_M, *, importance=None, ws=None, stream=None, check=False):
     """Packed importance [T] of B prompts: Q_la [B,N,L,H,d], K_prompt [L,H_kv,T,d], K_la [B,L,H_kv,N,d]."""
     import torch
     B, N, L, H, d = Q_la.shape
@@ -254,6 +261,7 @@ def score_varlen(Q_la, K_prompt, K_la, cu_M, *, importance=None, ws=None, stream
     ws = _workspace(need, K_prompt.device, ws)
     _check(sp_score_varlen(Q_la, K_prompt, K_la, B, cu, L, H, H_kv, d, N, dt, importance, ws, ws.numel(),
                            stream))
+    _check_device(ws, stream, check)
     return importance
 
 

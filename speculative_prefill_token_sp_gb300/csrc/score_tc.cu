@@ -11,29 +11,39 @@
 // resident).  Every CTA owns one fixed range of prompt tokens (multiples of 32)
 // in every (layer, KV head) slab, so the max over heads and layers of a token
 // stays inside one CTA: no atomics on the data path, and importance is written
-// once.  Warp roles:
+// once.  A row's weights can only be normalised once its lse over all M tokens
+// -- i.e. over every CTA -- is known, so each slab has a statistics pass (P1)
+// and, `lag` of its group's slabs later, a normalise pass (P2).  K is read from
+// HBM exactly once; the logits wait for P2 in TMEM.  Warp roles:
 //  * warp 0 (TMA): streams the CTA's K rows slab after slab (32-row x 128-byte
 //    boxes, 128B swizzle) through a ring of shared-memory stages, and the slab's
 //    query rows (a pre-swizzled image built by tc_prep_kernel) with one bulk copy;
 //  * warp 1 (MMA): tcgen05.mma, M = 128 tokens, N = 32 query rows (N*G padded),
-//    K = 16 per instruction, bf16 in, fp32 accumulate in TMEM; each slab has a
-//    TMEM slot holding all of the CTA's logits of that slab;
-//  * warps 2-9 (epilogue, two groups of four warps that split a slab's tiles,
-//    one TMEM lane per thread): per-row softmax statistics (max, sum of exp)
-//    over the CTA's tokens; `lag` slabs later the logits are read again from
-//    TMEM (not HBM), lse is subtracted, the max over the G heads of each
-//    look-ahead step is folded into a per-token running max in shared memory,
-//    and the TMEM slot goes back to the MMA warp;
+//    K = 16 per instruction, bf16 in, fp32 accumulate into a small "landing"
+//    ring of TMEM tiles per epilogue group;
+//  * warps 2-9 (epilogue, two independent groups of four warps; group g takes
+//    slabs g, g + 2, ...; one TMEM lane = one token per thread).  P1 reads a
+//    landing tile, frees it at once, reduces per-row softmax statistics (max,
+//    sum of exp) over the CTA's tokens, and stores the tile again in the
+//    group's "held" TMEM region as fp16 offsets from the tile's row maxima
+//    (half the columns, so many more slabs fit).  P2 reads the held tile,
+//    subtracts lse, takes the max over the G heads of each look-ahead step and
+//    folds it into a per-token running max in shared memory.  Held slabs never
+//    block the MMA warp, so the HBM stream does not wait for the lse exchange;
 //  * warp 10 (publish): writes the CTA's statistics of each slab to global
-//    memory and bumps the slab's counter (no fence: each entry is a single
-//    64-bit store and a published entry always has z >= 1, so readers can tell
-//    published entries from the zeroed ones);
-//  * warps 11-14 (merge): CTA c merges slabs s = c, c + P, ...: once the counter
-//    shows every CTA's statistics it reads them (re-reading any entry still 0),
-//    adds the look-ahead keys and publishes lse as (value, tag) 64-bit entries;
+//    memory (single 64-bit stores; a published entry always has z >= 1, so a
+//    zeroed entry means "not there yet" and no fence is needed);
+//  * warps 11-14 (merge): CTA c merges slabs s = c, c + P, ...: it reads every
+//    CTA's entry (re-reading those still 0), adds the look-ahead keys and
+//    publishes lse as (value, tag) 64-bit entries;
 //  * warp 15 (fetch): waits until a slab's lse entries are all tagged and copies
 //    them into a shared-memory ring for the epilogue.
-// K is read exactly once from HBM and the contraction runs once.
+//
+// Precision: P1 statistics use the fp32 logits.  P2 reads w = s - c in fp16,
+// c = the tile's row maximum, so w <= 0 and its rounding error is at most
+// |w| * 2^-11 (fp16 unit roundoff): a weight exp(w + c - lse) <= exp(w) is off by
+// at most |w| * 2^-11 relative (< 1% for w > -20) and by < 1.8e-4 absolute
+// (the maximum of exp(w) * |w| * 2^-11).
 //
 // Every wait is bounded: on timeout the kernel records SP_ETIMEOUT in the
 // workspace header, all roles stop, in-flight copies and MMAs are waited for
@@ -41,6 +51,7 @@
 #include "sp_common.cuh"
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -60,8 +71,9 @@ constexpr int kUnit = 32;            // token-range granularity
 constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 8;         // tiles per CTA per slab
-constexpr int kMaxSlots = 16;
-constexpr int kRing = 8;             // entries of the statistics and lse rings
+constexpr int kMaxHeld = 12;         // held slabs per epilogue group
+constexpr int kRing = 16;            // entries of the statistics and lse rings
+constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
 
@@ -70,19 +82,21 @@ struct TcParams {
     int S;              // slabs = L * H_kv
     int P;              // CTAs
     int U;              // 32-token units of the prompt
-    int n_tiles_max, slot_cols, NS, lag, tmem_cols, stages;
+    int n_tiles_max;
+    int land;           // landing tiles per epilogue group
+    int held;           // held slabs per epilogue group (lag + 1)
+    int lag;            // group-steps between a slab's P1 and its P2
+    int held_base;      // first TMEM column of the held regions
+    int stages;
     int64_t T;          // rows per slab in K (= M for one prompt)
-    int pf_bytes;       // bytes of K each CTA keeps requested into L2 ahead of its shared-memory loads
     float scale, scale_log2e;
-    const uint8_t* kbase;   // K_prompt
     // shared-memory carve (byte offsets from the 1024-aligned base)
-    int off_q, off_s, off_acc, off_x, off_stats, off_lse, off_bar, smem_bytes;
+    int off_q, off_s, off_acc, off_c, off_stats, off_lse, off_bar, smem_bytes;
     // workspace
     const uint8_t* qimg;            // [S][kRP * d] bf16, 128B-swizzled image of the slab's query rows
     const float2* la;               // [S][kRP] softmax statistics of the look-ahead keys
     unsigned long long* partials;   // [S][kRP][P] (m, z) as 64-bit words; 0 = not yet published
     unsigned long long* lse;        // [S][kRP] (lse bits, tag 1); 0 = not yet published
-    unsigned* cnt;                  // [S] CTAs that published a slab's statistics
     WsHeader* hdr;
     float* importance;
 };
@@ -127,6 +141,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase of `parity` to complete.  Returns false if the
 // kernel is aborting or the wait timed out (then the abort flag is raised).
+// Every barrier here has one waiter role that consumes its phases in order,
+// so a waiter is never more than one phase ahead of the barrier.
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr, int where) {
     unsigned long long t0 = 0;
     for (uint32_t i = 0;; ++i) {
@@ -144,12 +160,6 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
     }
 }
 
-__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ unsigned long long ld_cg64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.global.cg.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -158,12 +168,6 @@ __device__ __forceinline__ unsigned long long ld_cg64(const unsigned long long* 
 
 __device__ __forceinline__ void st64(unsigned long long* p, unsigned long long v) {
     asm volatile("st.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Release: the warp's earlier stores (ordered before this by __syncwarp) become
-// visible no later than the increment.
-__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long pack2(float a, float b) {
@@ -187,10 +191,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
@@ -204,6 +204,24 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void group_sync(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 __device__ __forceinline__ void merge_sync() { asm volatile("bar.sync 4, 128;" ::: "memory"); }
+
+// Barrier over `count` threads that also returns whether any of them passed
+// `c`: a stop decision taken from it is the same in every thread, so no thread
+// goes on to a barrier that the others have left.
+__device__ __forceinline__ bool bar_any(int id, int count, bool c) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 q, %2, 0;\n\t"
+        "bar.red.or.pred p, %1, %3, q;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(id), "r"((int)c), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool group_sync_any(int grp, bool c) { return bar_any(1 + grp, 128, c); }
+__device__ __forceinline__ bool merge_sync_any(bool c) { return bar_any(4, 128, c); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row groups 1024 bytes apart.
@@ -241,7 +259,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
+// 32 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     asm volatile(
@@ -257,6 +275,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Merge softmax statistics (m2, z2) into (m, z) (natural-log domain).
@@ -331,9 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
     uint8_t* k_stage = smem;                                       // [stages][kStageBytes]
     uint8_t* q_buf = smem + p.off_q;                               // [2][kQBytes]
-    float* Sbuf = reinterpret_cast<float*>(smem + p.off_s);        // [2 groups][2 buffers][kRP][4][33]
+    float* Sbuf = reinterpret_cast<float*>(smem + p.off_s);        // [2 groups][kRP][4][33]
     float* acc = reinterpret_cast<float*>(smem + p.off_acc);       // [2 groups][n_tiles_max][N][128]
-    float2* xchg = reinterpret_cast<float2*>(smem + p.off_x);      // [kRP] group 1 -> group 0
+    float* cbuf = reinterpret_cast<float*>(smem + p.off_c);        // [2 groups][held][n_tiles_max][kRP]
     float2* stats = reinterpret_cast<float2*>(smem + p.off_stats); // [kRing][kRP]
     float* lse_ring = reinterpret_cast<float*>(smem + p.off_lse);  // [kRing][kRP]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
@@ -341,16 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     uint64_t* k_empty = bars + p.stages;
     uint64_t* q_full = bars + 2 * p.stages;
     uint64_t* q_empty = q_full + 2;
-    uint64_t* slot_full = q_empty + 2;
-    uint64_t* slot_empty = slot_full + kMaxSlots;
-    uint64_t* stats_full = slot_empty + kMaxSlots;
+    uint64_t* land_full = q_empty + 2;             // [2 groups][land]
+    uint64_t* land_empty = land_full + 4;
+    uint64_t* stats_full = land_empty + 4;
     uint64_t* stats_empty = stats_full + kRing;
     uint64_t* lse_full = stats_empty + kRing;
     uint64_t* lse_empty = lse_full + kRing;
     uint64_t* final_bar = lse_empty + kRing;
-    uint64_t* merge_go = final_bar + 1;
-    volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(merge_go + 1);
+    volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(final_bar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+    volatile int* published = abort_flag + 1;      // slabs this CTA has published
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -361,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             mbar_init(smem_u32(&q_full[i]), 1);
             mbar_init(smem_u32(&q_empty[i]), 1);
         }
-        for (int i = 0; i < kMaxSlots; ++i) {
-            mbar_init(smem_u32(&slot_full[i]), 1);
-            mbar_init(smem_u32(&slot_empty[i]), 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(smem_u32(&land_full[i]), 1);
+            mbar_init(smem_u32(&land_empty[i]), 1);
         }
         for (int i = 0; i < kRing; ++i) {
             mbar_init(smem_u32(&stats_full[i]), 1);
@@ -372,13 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             mbar_init(smem_u32(&lse_empty[i]), 1);
         }
         mbar_init(smem_u32(final_bar), 1);
-        mbar_init(smem_u32(merge_go), 1);
         *abort_flag = 0;
+        *published = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32((const void*)tmem_base_sh)), "r"(p.tmem_cols)
+                     ::"r"(smem_u32((const void*)tmem_base_sh)), "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -394,16 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            // This CTA's rows of one slab are one contiguous byte range: keep the
-            // next `pf` slabs' ranges requested into L2 so that enough bytes are in
-            // flight per SM to cover the loaded memory latency; the shared-memory
-            // loads then hit L2.
-            const uint32_t slab_bytes = (uint32_t)len * D * 2;
-            const int pf = max(1, min(16, (int)((p.pf_bytes + slab_bytes - 1) / slab_bytes)));
-            for (int s = 0; s < min(pf, p.S); ++s)
-                prefetch_l2(p.kbase + ((size_t)s * p.T + t_begin) * D * 2, slab_bytes);
             for (int s = 0; s < p.S && ok; ++s) {
-                if (s + pf < p.S) prefetch_l2(p.kbase + ((size_t)(s + pf) * p.T + t_begin) * D * 2, slab_bytes);
                 const int qb = s & 1;
                 if (s >= 2) ok = mbar_wait(smem_u32(&q_empty[qb]), ((s >> 1) - 1) & 1, abort_flag, p.hdr, 1);
                 if (!ok) break;
@@ -438,23 +469,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             int it = 0;
+            int lt0 = 0, lt1 = 0;          // landing tiles written so far for each epilogue group
             bool ok = true;
             for (int s = 0; s < p.S && ok; ++s) {
-                const int slot = s % p.NS;
-                if (s >= p.NS) ok = mbar_wait(smem_u32(&slot_empty[slot]), ((s / p.NS) - 1) & 1, abort_flag, p.hdr, 3);
-                if (!ok) break;
-                tc_fence_after();
+                const int g = s & 1;       // the epilogue group that consumes slab s
                 const int qb = s & 1;
                 ok = mbar_wait(smem_u32(&q_full[qb]), (s >> 1) & 1, abort_flag, p.hdr, 4);
                 if (!ok) break;
                 const uint32_t qaddr = smem_u32(q_buf + qb * kQBytes);
                 for (int t = 0; t < n_tiles; ++t, ++it) {
-                    const int st = it % p.stages;
+                    const int lt = g ? lt1++ : lt0++;
+                    const int st = it % p.stages, slot = g * p.land + lt % p.land;
                     ok = mbar_wait(smem_u32(&k_full[st]), (it / p.stages) & 1, abort_flag, p.hdr, 5);
+                    if (ok && lt >= p.land)
+                        ok = mbar_wait(smem_u32(&land_empty[slot]), ((lt / p.land) - 1) & 1, abort_flag, p.hdr, 3);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(k_stage + (size_t)st * kStageBytes);
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(slot * p.slot_cols + t * kRP);
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(slot * kRP);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int hf = kk >> 2, ko = kk & 3;
@@ -463,10 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                         tc_mma(d_tmem, a, b, kIdesc, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&k_empty[st]));
+                    tc_commit(smem_u32(&land_full[slot]));
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&q_empty[qb]));
-                tc_commit(smem_u32(&slot_full[slot]));
             }
             // all MMAs issued so far complete before TMEM may be freed
             tc_commit(smem_u32(final_bar));
@@ -485,34 +517,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         const int tok = quad * 32 + lane;              // token row inside a tile
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
         const int r_e = ge >> 2, part = ge & 3;        // reduction role: row r_e, quarter `part`
-        float* S2 = Sbuf + grp * (2 * kRP * 4 * 33);   // two buffers per group, alternating by tile
+        float* S = Sbuf + grp * (kRP * 4 * 33);
         float* acc_g = acc + (size_t)grp * p.n_tiles_max * p.N * kTileRows;
-        int tb = 0;
-        bool ok = true;
+        float* cb_g = cbuf + (size_t)grp * p.held * p.n_tiles_max * kRP;
+        const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * p.n_tiles_max * 16);
         const int n_own = (p.S - grp + 1) / 2;         // slabs of this group
+        int lt = 0;                                    // landing tiles consumed so far
+        bool ok = true;
         for (int i = 0; i < n_own + p.lag && ok; ++i) {
-            // ---- statistics of this group's i-th slab ----
+            // ---- P1: statistics of this group's i-th slab, kept as fp16 offsets ----
             if (i < n_own) {
-                const int s = 2 * i + grp, slot = s % p.NS, q = s % kRing;
-                if (ge == 0) {
-                    mbar_wait(smem_u32(&slot_full[slot]), (s / p.NS) & 1, abort_flag, p.hdr, 6);
-                    if (s >= kRing) mbar_wait(smem_u32(&stats_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 7);
-                }
-                group_sync(grp);
-                if (*abort_flag) { ok = false; break; }
-                tc_fence_after();
+                const int s = 2 * i + grp, q = s % kRing, hs = i % p.held;
+                if (ge == 0 && s >= kRing)
+                    mbar_wait(smem_u32(&stats_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 7);
                 float m_run = -INFINITY, z_run = 0.f;
-                for (int t = 0; t < n_tiles; ++t) {
+                for (int t = 0; t < n_tiles; ++t, ++lt) {
+                    const int slot = grp * p.land + lt % p.land;
+                    if (ge == 0) mbar_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6);
+                    if (group_sync_any(grp, *abort_flag != 0)) { ok = false; break; }
+                    tc_fence_after();
                     float x[32];
-                    tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
+                    tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * kRP), x);
+                    tc_fence_before();
                     const bool valid = t * kTileRows + tok < len;
-                    // The buffer written here was last read two tiles ago; every thread
-                    // has passed this group's barrier of the tile in between since.
-                    float* S = S2 + tb * (kRP * 4 * 33);
-                    tb ^= 1;
 #pragma unroll
                     for (int r = 0; r < kRP; ++r) S[(r * 4 + quad) * 33 + lane] = valid ? x[r] : -INFINITY;
                     group_sync(grp);
+                    if (ge == 0) mbar_arrive(smem_u32(&land_empty[slot]));     // landing tile read by all
                     const float* row = S + (r_e * 4 + part) * 33;
                     float v[32];
 #pragma unroll
@@ -537,42 +568,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                         merge(m, z, m2, z2);
                     }
                     merge(m_run, z_run, m, z);
+                    // the tile's row maxima are the fp16 references of its held copy
+                    float* cb = cb_g + ((size_t)hs * p.n_tiles_max + t) * kRP;
+                    if (part == 0) cb[r_e] = m;
+                    group_sync(grp);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const __half2 h2 = __floats2half2_rn(fmaf(x[2 * k], p.scale, -cb[2 * k]),
+                                                             fmaf(x[2 * k + 1], p.scale, -cb[2 * k + 1]));
+                        pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    tmem_st16(held_g + (uint32_t)((hs * p.n_tiles_max + t) * 16), pk);
                 }
+                if (!ok) break;
                 if (part == 0) stats[q * kRP + r_e] = make_float2(m_run, z_run);
                 group_sync(grp);
                 if (ge == 0) mbar_arrive(smem_u32(&stats_full[q]));
             }
-            // ---- normalise + max of this group's (i - lag)-th slab ----
+            // ---- P2: normalise this group's (i - lag)-th slab, fold the max ----
             if (i >= p.lag) {
-                const int s = 2 * (i - p.lag) + grp, slot = s % p.NS, q = s % kRing;
+                const int i2 = i - p.lag;
+                const int s = 2 * i2 + grp, q = s % kRing, hs = i2 % p.held;
                 if (ge == 0) mbar_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8);
-                group_sync(grp);
-                if (*abort_flag) { ok = false; break; }
+                if (group_sync_any(grp, *abort_flag != 0)) { ok = false; break; }
                 float lr[kRP];
 #pragma unroll
                 for (int r = 0; r < kRP; ++r) lr[r] = lse_ring[q * kRP + r];
-                tc_fence_after();
                 for (int t = 0; t < n_tiles; ++t) {
-                    float x[32];
-                    tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * p.slot_cols + t * kRP), x);
+                    uint32_t pk[16];
+                    tmem_ld16(held_g + (uint32_t)((hs * p.n_tiles_max + t) * 16), pk);
+                    const float* cb = cb_g + ((size_t)hs * p.n_tiles_max + t) * kRP;
+                    float y[32];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
+                        y[2 * k] = f.x + (cb[2 * k] - lr[2 * k]);
+                        y[2 * k + 1] = f.y + (cb[2 * k + 1] - lr[2 * k + 1]);
+                    }
                     float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
 #pragma unroll
-                    for (int j = 0; j < kRP / G; ++j) {
-                        if (j < p.N) {
-                            float y = -INFINITY;
+                    for (int jj = 0; jj < kRP / G; ++jj) {
+                        if (jj < p.N) {
+                            float m = y[jj * G];
 #pragma unroll
-                            for (int hh = 0; hh < G; ++hh)
-                                y = fmaxf(y, fmaf(x[j * G + hh], p.scale, -lr[j * G + hh]));
-                            a[j * kTileRows] = fmaxf(a[j * kTileRows], y);
+                            for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jj * G + hh]);
+                            a[jj * kTileRows] = fmaxf(a[jj * kTileRows], m);
                         }
                     }
                 }
-                tc_fence_before();
-                group_sync(grp);
-                if (ge == 0) {
-                    mbar_arrive(smem_u32(&slot_empty[slot]));
-                    mbar_arrive(smem_u32(&lse_empty[q]));
-                }
+                group_sync(grp);                       // lse entry and references read by all
+                if (ge == 0) mbar_arrive(smem_u32(&lse_empty[q]));
             }
         }
         epi_sync();                                    // both groups' running maxima are complete
@@ -585,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 if (k < len) {
                     const float* a = acc + (size_t)t * p.N * kTileRows + tok;
                     float sum = 0.f;
-                    for (int j = 0; j < p.N; ++j) sum += expf(fmaxf(a[j * kTileRows], a[half + j * kTileRows]));
+                    for (int jj = 0; jj < p.N; ++jj) sum += expf(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows]));
                     p.importance[t_begin + k] = sum * inv_n;
                 }
             }
@@ -604,8 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(&stats_empty[q]));
-                // this CTA merges slab s: start reading the other CTAs' statistics now
-                if (s % p.P == c) mbar_arrive(smem_u32(merge_go));
+                *published = s + 1;        // wakes this CTA's merge warps for slab s if it is theirs
             }
         }
     } else if (warp < kFetchWarp) {
@@ -615,11 +660,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         // the entries are read until every CTA's is there.
         const int mi = threadIdx.x - kMergeBase;       // 0..127
         const int r = mi >> 2, part = mi & 3;
-        for (int s = c, k_go = 0; s < p.S; s += p.P, ++k_go) {
-            if (mi == 0) mbar_wait(smem_u32(merge_go), k_go & 1, abort_flag, p.hdr, 12);
-            merge_sync();
-            if (*abort_flag) break;
+        for (int s = c; s < p.S; s += p.P) {
+            if (mi == 0) {
+                const unsigned long long t0 = global_ns();
+                while (*published <= s) {
+                    if (*abort_flag) break;
+                    if (global_ns() - t0 > kTimeoutNs) {
+                        record_error(p.hdr, SP_ETIMEOUT, 12);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            if (merge_sync_any(*abort_flag != 0)) break;
             const unsigned long long* src = p.partials + ((size_t)s * kRP + r) * p.P;
+            const float2 la = __ldcg(&p.la[(size_t)s * kRP + r]);
             float m = -INFINITY, z = 0.f;
             bool ok = true;
             for (int base = part; base < p.P && ok; base += 128) {
@@ -669,8 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 merge(m, z, m2, z2);
             }
             if (part == 0) {
-                const float2 v = __ldcg(&p.la[(size_t)s * kRP + r]);
-                merge(m, z, v.x, v.y);
+                merge(m, z, la.x, la.y);
                 const float lse = m + __logf(z);
                 st64(&p.lse[(size_t)s * kRP + r], (unsigned long long)__float_as_uint(lse) | (1ull << 32));
             }
@@ -689,15 +744,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             unsigned long long v = ld_cg64(src);
             const unsigned long long t0 = global_ns();
             while (!__all_sync(0xffffffffu, (v >> 32) == 1ull)) {
-                if (*abort_flag) { ok = false; break; }
-                if (global_ns() - t0 > kTimeoutNs) {
-                    if (lane == 0) {
+                // lane 0 decides, so that the warp leaves the loop together
+                int stop = 0;
+                if (lane == 0) {
+                    if (*abort_flag) stop = 1;
+                    else if (global_ns() - t0 > kTimeoutNs) {
                         record_error(p.hdr, SP_ETIMEOUT, 11);
                         *abort_flag = 1;
+                        stop = 1;
                     }
-                    ok = false;
-                    break;
                 }
+                if (__shfl_sync(0xffffffffu, stop, 0)) { ok = false; break; }
                 __nanosleep(32);
                 v = ld_cg64(src);
             }
@@ -711,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -722,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
 struct Plan {
     TcParams p;
-    size_t off_qimg, off_la, off_partials, off_lse, off_cnt, total;
+    size_t off_qimg, off_la, off_partials, off_lse, total;
 };
 
 int sm_count_or(int fallback) {
@@ -758,54 +815,60 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     const int units_max = (p.U + p.P - 1) / p.P;
     p.n_tiles_max = (units_max * kUnit + kTileRows - 1) / kTileRows;
     if (p.n_tiles_max > kMaxTiles) return false;
-    p.slot_cols = p.n_tiles_max * kRP;
-    p.NS = std::min(kMaxSlots, 512 / p.slot_cols);
-    if (p.NS < 2) return false;
-    // slabs held between their statistics and their normalise pass; one more
-    // slot lets the MMA warp run a slab ahead when there are enough slots
-    // Each epilogue group holds lag + 1 of its own slabs (every other slab) in
-    // TMEM; with enough slots one more group-step lets the MMA warp run ahead.
-    p.NS &= ~1;
-    p.lag = p.NS >= 8 ? p.NS / 2 - 2 : p.NS / 2 - 1;
-    int cols = 32;
-    while (cols < p.NS * p.slot_cols) cols <<= 1;
-    p.tmem_cols = cols;
+    // TMEM: per epilogue group `land` fp32 landing tiles (32 columns each) and
+    // `held` slabs of fp16 tiles (16 columns each); two landing tiles when that
+    // still leaves room for at least two held slabs.
+    const int slab_cols = p.n_tiles_max * 16;
+    p.land = 2;
+    p.held = (kTmemCols / 2 - p.land * kRP) / slab_cols;
+    if (p.held < 2) {
+        p.land = 1;
+        p.held = (kTmemCols / 2 - p.land * kRP) / slab_cols;
+    }
+    if (p.held < 1) return false;
+    p.held = std::min(p.held, kMaxHeld);
+    p.lag = p.held - 1;
+    p.held_base = 2 * p.land * kRP;               // after both groups' landing tiles
+    if (p.held_base + 2 * p.held * slab_cols > kTmemCols) return false;
     p.scale = 1.0f / sqrtf((float)q.d);
     p.scale_log2e = p.scale * 1.4426950408889634f;
-    p.pf_bytes = 192 * 1024;
     const int stage_bytes = kTileRows * q.d * 2;
+    const int n_bars_max = 2 * 8 + 4 + 8 + 4 * kRing + 2;
+    const int c_bytes = 2 * p.held * p.n_tiles_max * kRP * 4;
     const int fixed = 2 * kRP * q.d * 2                      // query images
-                      + 4 * kRP * 4 * 33 * 4                  // reduction buffers (2 groups x 2)
+                      + 2 * kRP * 4 * 33 * 4                  // reduction buffers
                       + 2 * p.n_tiles_max * p.N * kTileRows * 4   // running max (one per group)
-                      + kRP * 8 + kRing * kRP * 8 + kRing * kRP * 4 + 16
-                      + (2 * 8 + 4 + 2 * kMaxSlots + 4 * kRing + 2) * 8 + 16 + 1024;
-    p.stages = std::min(8, (kSmemBudget - fixed) / stage_bytes);
+                      + c_bytes                               // fp16 references
+                      + kRing * kRP * 8 + kRing * kRP * 4 + 16
+                      + n_bars_max * 8 + 16 + 1024;
+    p.stages = std::min(6, (kSmemBudget - fixed) / stage_bytes);
     if (p.stages < 2) return false;
     int off = p.stages * stage_bytes;
     p.off_q = off;
     off += 2 * kRP * q.d * 2;
     p.off_s = off;
-    off += 4 * kRP * 4 * 33 * 4;
+    off += 2 * kRP * 4 * 33 * 4;
     p.off_acc = off;
     off += 2 * p.n_tiles_max * p.N * kTileRows * 4;
-    p.off_x = off;
-    off += kRP * 8;
+    p.off_c = off;
+    off += c_bytes;
     p.off_stats = off;
     off += kRing * kRP * 8;
     p.off_lse = off;
     off += kRing * kRP * 4;
     off = (off + 15) & ~15;
     p.off_bar = off;
-    off += (2 * p.stages + 4 + 2 * kMaxSlots + 4 * kRing + 2) * 8 + 16;
-    p.smem_bytes = off + 1024;                    // slack for 1024-byte alignment
+    off += (2 * p.stages + 4 + 8 + 4 * kRing + 2) * 8 + 16;
+    // slack for 1024-byte alignment; more than half of the SM's shared memory, so
+    // that one CTA runs per SM (each CTA allocates all 512 TMEM columns)
+    p.smem_bytes = std::max(off + 1024, 116 * 1024);
     if (p.smem_bytes > kSmemBudget) return false;
     // workspace (after the 256-byte header)
     Carve cv;
     const size_t S = (size_t)p.S;
     out.off_qimg = cv.take(S * kRP * q.d * 2);
     out.off_la = cv.take(S * kRP * sizeof(float2));
-    out.off_cnt = cv.take(S * sizeof(unsigned));          // cnt, lse, partials: zeroed per call
-    out.off_lse = cv.take(S * kRP * 8);
+    out.off_lse = cv.take(S * kRP * 8);                    // lse and partials are zeroed per call
     out.off_partials = cv.take(S * kRP * (size_t)kMaxCtas * 8);
     out.total = cv.off;
     return true;
@@ -887,9 +950,7 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     p.la = reinterpret_cast<const float2*>(w + plan.off_la);
     p.partials = reinterpret_cast<unsigned long long*>(w + plan.off_partials);
     p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
-    p.cnt = reinterpret_cast<unsigned*>(w + plan.off_cnt);
     p.importance = q.importance;
-    p.kbase = static_cast<const uint8_t*>(q.K);
 
     // K viewed as a 2D tensor of L*H_kv*T rows by d bf16 columns; 32-row x 64-column boxes.
     CUtensorMap map;
@@ -905,11 +966,11 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
         return SP_ECUDA;
     }
 
-    // zero the header, the counters, the tagged lse entries and the partial
-    // statistics this launch uses ([S][kRP][P] words)
+    // zero the header, the tagged lse entries and the partial statistics this
+    // launch uses ([S][kRP][P] words)
     SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
-    SP_CUDA_TRY(cudaMemsetAsync(w + plan.off_cnt, 0,
-                                plan.off_partials - plan.off_cnt + (size_t)p.S * kRP * p.P * 8, st));
+    SP_CUDA_TRY(cudaMemsetAsync(w + plan.off_lse, 0,
+                                plan.off_partials - plan.off_lse + (size_t)p.S * kRP * p.P * 8, st));
     tc_prep_kernel<<<p.S, 256, 0, st>>>(p, static_cast<const __nv_bfloat16*>(q.Q),
                                         static_cast<const __nv_bfloat16*>(q.Kla), w + plan.off_qimg,
                                         reinterpret_cast<float2*>(w + plan.off_la));

@@ -25,7 +25,7 @@ def sp():
 def run_score(sp, x):
     import torch
     Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
-    imp = sp.score(Q, K, Kla)
+    imp = sp.score(Q, K, Kla, check=True)
     torch.cuda.synchronize()
     return imp.cpu().numpy()
 
@@ -54,7 +54,7 @@ def test_varlen_config_parity(sp):
     import torch
     v = config_inputs(4)
     Q, K, Kla, cu = v.packed()
-    got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu)
+    got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu, check=True)
     torch.cuda.synchronize()
     got = got.cpu().numpy()
     refs = config_oracle(4)
@@ -87,6 +87,17 @@ def test_random_shapes(sp, shape):
     got = run_score(sp, x)
     ref = oracle.importance(x.Q_la, x.K_prompt, x.K_la)
     check_importance(got, ref, dt, str(shape))
+
+
+@pytest.mark.parametrize("M", [40960, 65536, 98305, 131072])
+def test_long_prompts_few_layers(sp, M):
+    """3 to 7 tiles of 128 tokens per CTA per slab and short look-behind (lag)
+    windows, on one layer of the 8B shape so that the oracle stays cheap."""
+    wl = W.Workload("t", L=1, H=32, H_kv=8, d=128, M=M, N=8, dtype="bf16", chunk=64, pool_k=3, mode="topk",
+                    keep_rate=0.1, needle_frac=0.01, run_min=16, run_max=128)
+    x = W.make_inputs(wl, seed=M)
+    got = run_score(sp, x)
+    check_importance(got, oracle.importance(x.Q_la, x.K_prompt, x.K_la), "bf16", f"M={M}")
 
 
 def test_varlen_ragged_with_empty_prompts(sp):
