@@ -13,37 +13,43 @@
 // stays inside one CTA: no atomics on the data path, and importance is written
 // once.  A row's weights can only be normalised once its lse over all M tokens
 // -- i.e. over every CTA -- is known, so each slab has a statistics pass (P1)
-// and, `lag` of its group's slabs later, a normalise pass (P2).  K is read from
+// and, `lag` slabs later, a normalise pass (P2).  K is read from
 // HBM exactly once; the logits wait for P2 in TMEM.  Warp roles:
-//  * warp 0 (TMA): streams the CTA's K rows slab after slab (32-row x 128-byte
-//    boxes, 128B swizzle) through a ring of shared-memory stages, and the slab's
-//    query rows (a pre-swizzled image built by tc_prep_kernel) with one bulk copy;
+//  * warp 0 (TMA): streams the CTA's K rows (32-row x 128-byte boxes, 128B
+//    swizzle) through a ring of shared-memory stages in plain order (slab after
+//    slab, so every CTA reads one sequential stream), and each slab's query rows
+//    (a pre-swizzled image built by tc_prep_kernel) with one bulk copy;
 //  * warp 1 (MMA): tcgen05.mma, M = 128 tokens, N = 32 query rows (N*G padded),
 //    K = 16 per instruction, bf16 in, fp32 accumulate into a small "landing"
-//    ring of TMEM tiles per epilogue group;
-//  * warps 2-9 (epilogue, two independent groups of four warps; group g takes
-//    slabs g, g + 2, ...; one TMEM lane = one token per thread).  P1 reads a
-//    landing tile, frees it at once, reduces per-row softmax statistics (max,
-//    sum of exp) over the CTA's tokens, and stores the tile again in the
-//    group's "held" TMEM region as fp16 offsets from the tile's row maxima
-//    (half the columns, so many more slabs fit).  P2 reads the held tile,
-//    subtracts lse, takes the max over the G heads of each look-ahead step and
-//    folds it into a per-token running max in shared memory.  Held slabs never
-//    block the MMA warp, so the HBM stream does not wait for the lse exchange;
-//  * warp 10 (publish): writes the CTA's statistics of each slab to global
-//    memory (single 64-bit stores; a published entry always has z >= 1, so a
-//    zeroed entry means "not there yet" and no fence is needed);
-//  * warps 11-14 (merge): CTA c merges slabs s = c, c + P, ...: it reads every
+//    ring of TMEM tiles per epilogue group; the CTA's k-th tile goes to group
+//    k % 2, so both groups work on every slab;
+//  * warps 2-17 (epilogue, two groups of eight warps; one TMEM lane = one token
+//    per thread).  Each warp owns one TMEM lane quadrant (32 tokens of every
+//    tile) and one half of the query rows, and works on it alone: its hand-offs
+//    are mbarriers that count the warps taking part, never a barrier with
+//    another warp.  P1 reads its part of a landing tile, frees it at once,
+//    reduces per-row softmax statistics (max, sum of exp) over its 32 tokens
+//    through a warp-private transpose, and stores the part again in the group's
+//    "held" TMEM region as fp16 offsets from the quadrant's row maxima (half the
+//    columns, so many more slabs fit).  P2 reads the held part, subtracts lse,
+//    takes the max over the G heads of each look-ahead step and folds it into a
+//    per-token running max in shared memory.  Held slabs never block the MMA
+//    warp, so the HBM stream does not wait for the lse exchange;
+//  * warp 18 (publish): merges the eight parts' statistics of each slab and
+//    writes them to global memory (single 64-bit stores; a published entry
+//    always has z >= 1, so a zeroed entry means "not there yet" and no fence is
+//    needed);
+//  * warps 19-22 (merge): CTA c merges slabs s = c, c + P, ...: it reads every
 //    CTA's entry (re-reading those still 0), adds the look-ahead keys and
 //    publishes lse as (value, tag) 64-bit entries;
-//  * warp 15 (fetch): waits until a slab's lse entries are all tagged and copies
+//  * warp 23 (fetch): waits until a slab's lse entries are all tagged and copies
 //    them into a shared-memory ring for the epilogue.
 //
 // Precision: P1 statistics use the fp32 logits.  P2 reads w = s - c in fp16,
-// c = the tile's row maximum, so w <= 0 and its rounding error is at most
-// |w| * 2^-11 (fp16 unit roundoff): a weight exp(w + c - lse) <= exp(w) is off by
-// at most |w| * 2^-11 relative (< 1% for w > -20) and by < 1.8e-4 absolute
-// (the maximum of exp(w) * |w| * 2^-11).
+// c = the row maximum over the warp's 32 tokens of the tile, so w <= 0 and its
+// rounding error is at most |w| * 2^-11 (fp16 unit roundoff): a weight
+// exp(w + c - lse) <= exp(w) is off by at most |w| * 2^-11 relative (< 1% for
+// w > -20) and by < 1.8e-4 absolute (the maximum of exp(w) * |w| * 2^-11).
 //
 // Every wait is bounded: on timeout the kernel records SP_ETIMEOUT in the
 // workspace header, all roles stop, in-flight copies and MMAs are waited for
@@ -60,11 +66,11 @@
 namespace sp {
 namespace {
 
-constexpr int kThreads = 512;        // 16 warps
-constexpr int kEpiBase = 64;         // warps 2-9: epilogue
-constexpr int kPubWarp = 10;
-constexpr int kMergeBase = 352;      // warps 11-14: merge
-constexpr int kFetchWarp = 15;
+constexpr int kThreads = 768;        // 24 warps
+constexpr int kPubWarp = 18;         // warps 2-17: epilogue
+constexpr int kMergeBase = 608;      // warps 19-22: merge
+constexpr int kFetchWarp = 23;
+constexpr int kEpiWarpsPerGroup = 8;
 constexpr int kTileRows = 128;       // tokens per MMA tile (MMA M)
 constexpr int kBoxRows = 32;         // rows per TMA box
 constexpr int kUnit = 32;            // token-range granularity
@@ -72,7 +78,10 @@ constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 8;         // tiles per CTA per slab
 constexpr int kMaxHeld = 12;         // held slabs per epilogue group
-constexpr int kRing = 16;            // entries of the statistics and lse rings
+constexpr int kRing = 16;            // entries of the lse ring
+constexpr int kStatsRing = 4;        // entries of the statistics ring
+constexpr int kMaxQ = 4;             // query-image buffers
+constexpr int kMaxLand = 4;          // landing tiles per epilogue group
 constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
@@ -84,10 +93,12 @@ struct TcParams {
     int U;              // 32-token units of the prompt
     int n_tiles_max;
     int land;           // landing tiles per epilogue group
-    int held;           // held slabs per epilogue group (lag + 1)
-    int lag;            // group-steps between a slab's P1 and its P2
+    int tiles_per_group;  // tiles of one slab an epilogue group takes, at most
+    int held;           // held slabs (lag + 1)
+    int lag;            // slabs between a slab's P1 and its P2
     int held_base;      // first TMEM column of the held regions
     int stages;
+    int nq;             // query-image buffers (2 or 4)
     int64_t T;          // rows per slab in K (= M for one prompt)
     float scale, scale_log2e;
     // shared-memory carve (byte offsets from the 1024-aligned base)
@@ -139,23 +150,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended (without issuing) for up
+// to `hint_ns` while the phase is incomplete; it resumes when the phase
+// completes.  Waiting threads then take no issue slots from the working warps.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete.  Returns false if the
 // kernel is aborting or the wait timed out (then the abort flag is raised).
-// Every barrier here has one waiter role that consumes its phases in order,
-// so a waiter is never more than one phase ahead of the barrier.
+// Every waiter consumes a barrier's phases in order, and the producer of phase
+// k + 1 first needs every waiter's hand-off of phase k, so a waiter is never
+// more than one phase ahead of the barrier.
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr, int where) {
-    unsigned long long t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 1000u)) return true;
         if (*abort_flag) return false;
-        if ((i & 63u) == 0) {
-            unsigned long long t = global_ns();
-            if (i == 0) t0 = t;
-            else if (t - t0 > kTimeoutNs) {
-                record_error(hdr, SP_ETIMEOUT, where);
-                *abort_flag = 1;
-                return false;
-            }
+        if (global_ns() - t0 > kTimeoutNs) {
+            record_error(hdr, SP_ETIMEOUT, where);
+            *abort_flag = 1;
+            return false;
         }
     }
 }
@@ -200,9 +224,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Named barriers: 1 and 2 = the two epilogue groups, 3 = whole epilogue, 4 = merge warps.
-__device__ __forceinline__ void group_sync(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+// Named barriers: 3 = the eight epilogue warps (once, at the end), 4 = merge warps.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, 512;" ::: "memory"); }
 __device__ __forceinline__ void merge_sync() { asm volatile("bar.sync 4, 128;" ::: "memory"); }
 
 // Barrier over `count` threads that also returns whether any of them passed
@@ -220,7 +243,6 @@ __device__ __forceinline__ bool bar_any(int id, int count, bool c) {
         : "memory");
     return r != 0;
 }
-__device__ __forceinline__ bool group_sync_any(int grp, bool c) { return bar_any(1 + grp, 128, c); }
 __device__ __forceinline__ bool merge_sync_any(bool c) { return bar_any(4, 128, c); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -259,26 +281,9 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
-// 32 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 16 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// 16 consecutive 32-bit columns of this thread's TMEM lane, as floats.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -287,14 +292,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -309,14 +323,25 @@ __device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-call preparation: swizzled query images and look-ahead statistics.
+// Per-call preparation (one block per slab): the swizzled query image, the
+// softmax statistics of the look-ahead keys, and the zeroed exchange entries
+// (a zero word means "not published yet"); block 0 also clears the status.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __nv_bfloat16* __restrict__ Q,
                                                       const __nv_bfloat16* __restrict__ Kla,
-                                                      uint8_t* __restrict__ qimg, float2* __restrict__ la) {
+                                                      uint8_t* __restrict__ qimg, float2* __restrict__ la,
+                                                      unsigned long long* __restrict__ lse,
+                                                      unsigned long long* __restrict__ partials, WsHeader* hdr) {
     const int s = blockIdx.x;
     const int l = s / p.H_kv, g = s % p.H_kv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
+    if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
+    {
+        unsigned long long* ps = partials + (size_t)s * kRP * p.P;
+        for (int i = threadIdx.x; i < kRP * p.P; i += blockDim.x) ps[i] = 0ull;
+    }
     const int cpr = p.d / 8;                      // 16-byte chunks per row
     uint8_t* img = qimg + (size_t)s * kRP * p.d * 2;
     for (int idx = threadIdx.x; idx < kRP * cpr; idx += blockDim.x) {
@@ -330,7 +355,9 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
         const size_t off = (size_t)half * (kRP * 128) + (size_t)r * 128 + (size_t)((c ^ (r & 7)) * 16);
         *reinterpret_cast<uint4*>(img + off) = v;
     }
-    for (int r = threadIdx.x; r < kRP; r += blockDim.x) {
+    // row r (query j = r / G, head g*G + r % G) against look-ahead keys k <= j:
+    // one warp per row, lanes split the dot product
+    for (int r = warp; r < kRP; r += blockDim.x / 32) {
         float m = -INFINITY, z = 0.f;
         if (r < p.R) {
             const int j = r / p.G, h = g * p.G + r % p.G;
@@ -338,17 +365,30 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
             for (int k = 0; k <= j; ++k) {
                 const __nv_bfloat16* kk = Kla + (((size_t)l * p.H_kv + g) * p.N + k) * p.d;
                 float u = 0.f;
-                for (int t = 0; t < p.d; ++t) u = fmaf(__bfloat162float(q[t]), __bfloat162float(kk[t]), u);
+                for (int t = lane; t < p.d; t += 32) u = fmaf(__bfloat162float(q[t]), __bfloat162float(kk[t]), u);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
                 merge(m, z, u * p.scale, 1.f);
             }
         }
-        la[(size_t)s * kRP + r] = make_float2(m, z);
+        if (lane == 0) la[(size_t)s * kRP + r] = make_float2(m, z);
     }
 }
 
 // ---------------------------------------------------------------------------
 // The persistent scoring kernel
 // ---------------------------------------------------------------------------
+
+// Lane 0 of the warp waits for the barrier phase; the outcome is shared with
+// the whole warp, which then leaves or goes on together.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
+                                          int where) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, hdr, where) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -370,22 +410,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     const int n_tiles = (len + kTileRows - 1) / kTileRows;
 
     uint8_t* k_stage = smem;                                       // [stages][kStageBytes]
-    uint8_t* q_buf = smem + p.off_q;                               // [2][kQBytes]
-    float* Sbuf = reinterpret_cast<float*>(smem + p.off_s);        // [2 groups][kRP][4][33]
+    uint8_t* q_buf = smem + p.off_q;                               // [nq][kQBytes]
+    float* wbuf = reinterpret_cast<float*>(smem + p.off_s);        // [16 epilogue warps][16][33]
     float* acc = reinterpret_cast<float*>(smem + p.off_acc);       // [2 groups][n_tiles_max][N][128]
-    float* cbuf = reinterpret_cast<float*>(smem + p.off_c);        // [2 groups][held][n_tiles_max][kRP]
-    float2* stats = reinterpret_cast<float2*>(smem + p.off_stats); // [kRing][kRP]
+    float* cbuf = reinterpret_cast<float*>(smem + p.off_c);        // [2 groups][held][tiles_per_group][4][kRP]
+    float2* stats = reinterpret_cast<float2*>(smem + p.off_stats); // [kStatsRing][2 groups][4][kRP]
     float* lse_ring = reinterpret_cast<float*>(smem + p.off_lse);  // [kRing][kRP]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* k_full = bars;
     uint64_t* k_empty = bars + p.stages;
-    uint64_t* q_full = bars + 2 * p.stages;
-    uint64_t* q_empty = q_full + 2;
-    uint64_t* land_full = q_empty + 2;             // [2 groups][land]
-    uint64_t* land_empty = land_full + 4;
-    uint64_t* stats_full = land_empty + 4;
-    uint64_t* stats_empty = stats_full + kRing;
-    uint64_t* lse_full = stats_empty + kRing;
+    uint64_t* q_full = bars + 2 * p.stages;        // [kMaxQ]
+    uint64_t* q_empty = q_full + kMaxQ;
+    uint64_t* land_full = q_empty + kMaxQ;         // [2 groups][kMaxLand]
+    uint64_t* land_empty = land_full + 2 * kMaxLand;
+    uint64_t* stats_full = land_empty + 2 * kMaxLand;   // [kStatsRing]
+    uint64_t* stats_empty = stats_full + kStatsRing;
+    uint64_t* lse_full = stats_empty + kStatsRing; // [kRing]
     uint64_t* lse_empty = lse_full + kRing;
     uint64_t* final_bar = lse_empty + kRing;
     volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(final_bar + 2);
@@ -397,19 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             mbar_init(smem_u32(&k_full[i]), 1);
             mbar_init(smem_u32(&k_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMaxQ; ++i) {
             mbar_init(smem_u32(&q_full[i]), 1);
             mbar_init(smem_u32(&q_empty[i]), 1);
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2 * kMaxLand; ++i) {
             mbar_init(smem_u32(&land_full[i]), 1);
-            mbar_init(smem_u32(&land_empty[i]), 1);
+            mbar_init(smem_u32(&land_empty[i]), kEpiWarpsPerGroup);   // one arrival per epilogue warp of the group
+        }
+        for (int i = 0; i < kStatsRing; ++i) {
+            mbar_init(smem_u32(&stats_full[i]), 2 * kEpiWarpsPerGroup);   // every epilogue warp
+            mbar_init(smem_u32(&stats_empty[i]), 1);
         }
         for (int i = 0; i < kRing; ++i) {
-            mbar_init(smem_u32(&stats_full[i]), 1);
-            mbar_init(smem_u32(&stats_empty[i]), 1);
             mbar_init(smem_u32(&lse_full[i]), 1);
-            mbar_init(smem_u32(&lse_empty[i]), 1);
+            mbar_init(smem_u32(&lse_empty[i]), 2 * kEpiWarpsPerGroup);
         }
         mbar_init(smem_u32(final_bar), 1);
         *abort_flag = 0;
@@ -429,14 +471,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_sh;
 
+    // Every CTA streams its tiles in plain order: slab after slab, the slab's
+    // tiles in order (k = s * n_tiles + t).  Tile k goes to epilogue group k % 2,
+    // so both groups work on every slab and the HBM stream stays sequential.
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             int it = 0;
             bool ok = true;
             for (int s = 0; s < p.S && ok; ++s) {
-                const int qb = s & 1;
-                if (s >= 2) ok = mbar_wait(smem_u32(&q_empty[qb]), ((s >> 1) - 1) & 1, abort_flag, p.hdr, 1);
+                const int qb = s % p.nq;
+                if (s >= p.nq) ok = mbar_wait(smem_u32(&q_empty[qb]), ((s / p.nq) - 1) & 1, abort_flag, p.hdr, 1);
                 if (!ok) break;
                 mbar_expect_tx(smem_u32(&q_full[qb]), kQBytes);
                 bulk_load(smem_u32(q_buf + qb * kQBytes), p.qimg + (size_t)s * kQBytes, kQBytes,
@@ -472,17 +517,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             int lt0 = 0, lt1 = 0;          // landing tiles written so far for each epilogue group
             bool ok = true;
             for (int s = 0; s < p.S && ok; ++s) {
-                const int g = s & 1;       // the epilogue group that consumes slab s
-                const int qb = s & 1;
-                ok = mbar_wait(smem_u32(&q_full[qb]), (s >> 1) & 1, abort_flag, p.hdr, 4);
+                const int qb = s % p.nq;
+                ok = mbar_wait(smem_u32(&q_full[qb]), (s / p.nq) & 1, abort_flag, p.hdr, 4);
                 if (!ok) break;
                 const uint32_t qaddr = smem_u32(q_buf + qb * kQBytes);
                 for (int t = 0; t < n_tiles; ++t, ++it) {
-                    const int lt = g ? lt1++ : lt0++;
-                    const int st = it % p.stages, slot = g * p.land + lt % p.land;
+                    const int g = it & 1;          // epilogue group of tile k = it
+                    const int l = g ? lt1++ : lt0++;
+                    const int st = it % p.stages, slot = g * p.land + l % p.land;
                     ok = mbar_wait(smem_u32(&k_full[st]), (it / p.stages) & 1, abort_flag, p.hdr, 5);
-                    if (ok && lt >= p.land)
-                        ok = mbar_wait(smem_u32(&land_empty[slot]), ((lt / p.land) - 1) & 1, abort_flag, p.hdr, 3);
+                    if (ok && l >= p.land)
+                        ok = mbar_wait(smem_u32(&land_empty[slot]), ((l / p.land) - 1) & 1, abort_flag, p.hdr, 3);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(k_stage + (size_t)st * kStageBytes);
@@ -509,120 +554,136 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         __syncwarp();
     } else if (warp < kPubWarp) {
         // ------------------------------ epilogue ------------------------------
-        // Two independent groups of four warps: group g handles slabs g, g + 2, ...
-        // with its own barrier, so one group's waits overlap the other's work.
-        const int e = threadIdx.x - kEpiBase;          // 0..255
-        const int grp = e >> 7, ge = e & 127;
+        // Sixteen warps, two groups of eight; group g takes the tiles k with
+        // k % 2 == g (k = s * n_tiles + t), so both groups work on every slab.
+        // A warp owns one TMEM lane quadrant (32 tokens of every tile) and one
+        // half of the query rows (16 of the 32 columns), and works on it alone:
+        // statistics and fp16 references are per (quadrant, row), and the
+        // hand-offs to the other roles are mbarriers that count the warps taking
+        // part, so no warp ever waits at a barrier for another.
+        const int ew = warp - 2;                       // 0..15
+        const int grp = ew >> 3;
         const int quad = warp & 3;                     // TMEM lane quadrant of this warp
+        const int rh = (ew >> 2) & 1;                  // query rows rh*16 .. rh*16 + 15
         const int tok = quad * 32 + lane;              // token row inside a tile
+        const int row = lane & 15, th = lane >> 4;     // reduction role: row, 16-token half
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        const int r_e = ge >> 2, part = ge & 3;        // reduction role: row r_e, quarter `part`
-        float* S = Sbuf + grp * (kRP * 4 * 33);
+        const int tpg = p.tiles_per_group;             // held tile slots per slab
+        float* wp = wbuf + ew * (16 * 33);             // this warp's transpose buffer
         float* acc_g = acc + (size_t)grp * p.n_tiles_max * p.N * kTileRows;
-        float* cb_g = cbuf + (size_t)grp * p.held * p.n_tiles_max * kRP;
-        const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * p.n_tiles_max * 16);
-        const int n_own = (p.S - grp + 1) / 2;         // slabs of this group
+        float* cb_g = cbuf + (size_t)grp * p.held * tpg * 4 * kRP;
+        const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * tpg * 16 + rh * 8);
+        const int odd = n_tiles & 1;
         int lt = 0;                                    // landing tiles consumed so far
         bool ok = true;
-        for (int i = 0; i < n_own + p.lag && ok; ++i) {
-            // ---- P1: statistics of this group's i-th slab, kept as fp16 offsets ----
-            if (i < n_own) {
-                const int s = 2 * i + grp, q = s % kRing, hs = i % p.held;
-                if (ge == 0 && s >= kRing)
-                    mbar_wait(smem_u32(&stats_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 7);
+        for (int i = 0; i < p.S + p.lag && ok; ++i) {
+            // ---- P1: statistics of slab i over this group's tiles, kept as fp16 offsets ----
+            if (i < p.S) {
+                const int s = i, q = s % kStatsRing, hs = s % p.held;
+                const int t0 = (grp + s * odd) & 1;    // this group's first tile of the slab
+                if (s >= kStatsRing &&
+                    !warp_wait(smem_u32(&stats_empty[q]), ((s / kStatsRing) - 1) & 1, abort_flag, p.hdr, 7)) {
+                    ok = false;
+                    break;
+                }
+                // lanes row and row + 16: running statistics of query row rh*16 + row
+                // over this quadrant's tokens (same m_run in both, z_run per half)
                 float m_run = -INFINITY, z_run = 0.f;
-                for (int t = 0; t < n_tiles; ++t, ++lt) {
+                for (int t = t0, j = 0; t < n_tiles; t += 2, ++j, ++lt) {
                     const int slot = grp * p.land + lt % p.land;
-                    if (ge == 0) mbar_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6);
-                    if (group_sync_any(grp, *abort_flag != 0)) { ok = false; break; }
+                    if (!warp_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    float x[32];
-                    tmem_ld32(tmem_base + lane_addr + (uint32_t)(slot * kRP), x);
+                    float x[16];
+                    tmem_ld16f(tmem_base + lane_addr + (uint32_t)(slot * kRP + rh * 16), x);
                     tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));    // this part is read
                     const bool valid = t * kTileRows + tok < len;
 #pragma unroll
-                    for (int r = 0; r < kRP; ++r) S[(r * 4 + quad) * 33 + lane] = valid ? x[r] : -INFINITY;
-                    group_sync(grp);
-                    if (ge == 0) mbar_arrive(smem_u32(&land_empty[slot]));     // landing tile read by all
-                    const float* row = S + (r_e * 4 + part) * 33;
-                    float v[32];
+                    for (int r = 0; r < 16; ++r) wp[r * 33 + lane] = valid ? x[r] : -INFINITY;
+                    __syncwarp();
+                    float v[16];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = row[k];
+                    for (int k = 0; k < 16; ++k) v[k] = wp[row * 33 + th * 16 + k];
                     float mq[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-                    for (int k = 4; k < 32; ++k) mq[k & 3] = fmaxf(mq[k & 3], v[k]);
-                    const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-                    float z = 0.f;
-                    if (mx != -INFINITY) {
-                        const float off = mx * p.scale_log2e;
+                    for (int k = 4; k < 16; ++k) mq[k & 3] = fmaxf(mq[k & 3], v[k]);
+                    float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_t = mx == -INFINITY ? -INFINITY : mx * p.scale;
+                    const float m_new = fmaxf(m_run, m_t);
+                    if (m_new != -INFINITY) {
+                        const float off = m_new * 1.4426950408889634f;
                         float zq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) zq[k & 3] += ex2_approx(fmaf(v[k], p.scale_log2e, -off));
-                        z = (zq[0] + zq[1]) + (zq[2] + zq[3]);
+                        for (int k = 0; k < 16; ++k) zq[k & 3] += ex2_approx(fmaf(v[k], p.scale_log2e, -off));
+                        const float zt = (zq[0] + zq[1]) + (zq[2] + zq[3]);
+                        z_run = (m_run == -INFINITY ? 0.f : z_run * ex2_approx((m_run - m_new) * 1.4426950408889634f)) + zt;
+                        m_run = m_new;
                     }
-                    float m = mx == -INFINITY ? -INFINITY : mx * p.scale;
+                    // the quadrant's row maxima are the fp16 references of its held copy
+                    float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
+                    if (th == 0) cq[row] = m_t == -INFINITY ? 0.f : m_t;
+                    __syncwarp();
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int o = 1; o <= 2; o <<= 1) {
-                        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-                        const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
-                        merge(m, z, m2, z2);
-                    }
-                    merge(m_run, z_run, m, z);
-                    // the tile's row maxima are the fp16 references of its held copy
-                    float* cb = cb_g + ((size_t)hs * p.n_tiles_max + t) * kRP;
-                    if (part == 0) cb[r_e] = m;
-                    group_sync(grp);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const __half2 h2 = __floats2half2_rn(fmaf(x[2 * k], p.scale, -cb[2 * k]),
-                                                             fmaf(x[2 * k + 1], p.scale, -cb[2 * k + 1]));
+                    for (int k = 0; k < 8; ++k) {
+                        const __half2 h2 = __floats2half2_rn(fmaf(x[2 * k], p.scale, -cq[2 * k]),
+                                                             fmaf(x[2 * k + 1], p.scale, -cq[2 * k + 1]));
                         pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
-                    tmem_st16(held_g + (uint32_t)((hs * p.n_tiles_max + t) * 16), pk);
+                    tmem_st8(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
                 }
                 if (!ok) break;
-                if (part == 0) stats[q * kRP + r_e] = make_float2(m_run, z_run);
-                group_sync(grp);
-                if (ge == 0) mbar_arrive(smem_u32(&stats_full[q]));
+                const float z = z_run + __shfl_xor_sync(0xffffffffu, z_run, 16);
+                if (th == 0) stats[((q * 2 + grp) * 4 + quad) * kRP + rh * 16 + row] = make_float2(m_run, z);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&stats_full[q]));
             }
-            // ---- P2: normalise this group's (i - lag)-th slab, fold the max ----
+            // ---- P2: normalise this group's tiles of slab i - lag, fold the max ----
             if (i >= p.lag) {
-                const int i2 = i - p.lag;
-                const int s = 2 * i2 + grp, q = s % kRing, hs = i2 % p.held;
-                if (ge == 0) mbar_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8);
-                if (group_sync_any(grp, *abort_flag != 0)) { ok = false; break; }
-                float lr[kRP];
+                const int s = i - p.lag, q = s % kRing, hs = s % p.held;
+                const int t0 = (grp + s * odd) & 1;
+                if (!warp_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8)) {
+                    ok = false;
+                    break;
+                }
+                float lr[16];
 #pragma unroll
-                for (int r = 0; r < kRP; ++r) lr[r] = lse_ring[q * kRP + r];
-                for (int t = 0; t < n_tiles; ++t) {
-                    uint32_t pk[16];
-                    tmem_ld16(held_g + (uint32_t)((hs * p.n_tiles_max + t) * 16), pk);
-                    const float* cb = cb_g + ((size_t)hs * p.n_tiles_max + t) * kRP;
-                    float y[32];
+                for (int r = 0; r < 16; ++r) lr[r] = lse_ring[q * kRP + rh * 16 + r];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&lse_empty[q]));
+                for (int t = t0, j = 0; t < n_tiles; t += 2, ++j) {
+                    uint32_t pk[8];
+                    tmem_ld8(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
+                    const float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
+                    float y[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
+                    for (int k = 0; k < 8; ++k) {
                         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
-                        y[2 * k] = f.x + (cb[2 * k] - lr[2 * k]);
-                        y[2 * k + 1] = f.y + (cb[2 * k + 1] - lr[2 * k + 1]);
+                        y[2 * k] = f.x + (cq[2 * k] - lr[2 * k]);
+                        y[2 * k + 1] = f.y + (cq[2 * k + 1] - lr[2 * k + 1]);
                     }
+                    // rows rh*16 + k are look-ahead steps jj = rh*(16/G) + k/G, heads k%G
                     float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
 #pragma unroll
-                    for (int jj = 0; jj < kRP / G; ++jj) {
+                    for (int jl = 0; jl < 16 / G; ++jl) {
+                        const int jj = rh * (16 / G) + jl;
                         if (jj < p.N) {
-                            float m = y[jj * G];
+                            float m = y[jl * G];
 #pragma unroll
-                            for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jj * G + hh]);
+                            for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jl * G + hh]);
                             a[jj * kTileRows] = fmaxf(a[jj * kTileRows], m);
                         }
                     }
                 }
-                group_sync(grp);                       // lse entry and references read by all
-                if (ge == 0) mbar_arrive(smem_u32(&lse_empty[q]));
             }
         }
         epi_sync();                                    // both groups' running maxima are complete
-        if (!*abort_flag) {
+        if (!*abort_flag && rh == 0) {
             // importance of this CTA's tokens: (1/N) sum_j exp(max_{l,h}(s - lse))
             const float inv_n = 1.0f / (float)p.N;
             const size_t half = (size_t)p.n_tiles_max * p.N * kTileRows;
@@ -638,20 +699,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         }
     } else if (warp == kPubWarp) {
         // ------------------------------ publish ------------------------------
+        // lane r merges row r's statistics over the two groups and four
+        // quadrants and writes them to global memory as one 64-bit word.
         for (int s = 0; s < p.S; ++s) {
-            const int q = s % kRing;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(smem_u32(&stats_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 9);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            __syncwarp();
-            if (!ok) break;
-            const float2 v = stats[q * kRP + lane];
-            st64(&p.partials[((size_t)s * kRP + lane) * p.P + c], pack2(v.x, v.y));
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&stats_empty[q]));
-                *published = s + 1;        // wakes this CTA's merge warps for slab s if it is theirs
+            const int q = s % kStatsRing;
+            if (!warp_wait(smem_u32(&stats_full[q]), (s / kStatsRing) & 1, abort_flag, p.hdr, 9)) break;
+            float m = -INFINITY, z = 0.f;
+#pragma unroll
+            for (int part = 0; part < 8; ++part) {
+                const float2 v = stats[(q * 8 + part) * kRP + lane];
+                merge(m, z, v.x, v.y);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&stats_empty[q]));
+            st64(&p.partials[((size_t)s * kRP + lane) * p.P + c], pack2(m, z));
+            __syncwarp();
+            if (lane == 0) *published = s + 1;      // wakes this CTA's merge warps for slab s if it is theirs
         }
     } else if (warp < kFetchWarp) {
         // ------------------------------ merge ------------------------------
@@ -678,11 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             const float2 la = __ldcg(&p.la[(size_t)s * kRP + r]);
             float m = -INFINITY, z = 0.f;
             bool ok = true;
-            for (int base = part; base < p.P && ok; base += 128) {
-                // all loads of the batch first (up to 32 in flight per thread)
-                unsigned long long v[32];
+            for (int base = part; base < p.P && ok; base += 64) {
+                // all loads of the batch first (up to 16 in flight per thread)
+                unsigned long long v[16];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
+                for (int k = 0; k < 16; ++k) {
                     const int cc = base + 4 * k;
                     v[k] = cc < p.P ? ld_cg64(src + cc) : 0ull;
                 }
@@ -692,22 +755,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 for (;;) {
                     bool missing = false;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
+                    for (int k = 0; k < 16; ++k)
                         if (base + 4 * k < p.P && (v[k] >> 32) == 0ull) missing = true;
                     if (!missing) break;
                     if (*abort_flag || global_ns() - t0 > kTimeoutNs) { ok = false; break; }
                     __nanosleep(64);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
+                    for (int k = 0; k < 16; ++k)
                         if (base + 4 * k < p.P && (v[k] >> 32) == 0ull) v[k] = ld_cg64(src + base + 4 * k);
                 }
                 float mb = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
+                for (int k = 0; k < 16; ++k)
                     if (base + 4 * k < p.P) mb = fmaxf(mb, unpack2(v[k]).x);
                 float zb = 0.f;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
+                for (int k = 0; k < 16; ++k) {
                     if (base + 4 * k >= p.P) continue;
                     const float2 f = unpack2(v[k]);
                     zb += f.y * __expf(f.x - mb);
@@ -816,9 +879,10 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     p.n_tiles_max = (units_max * kUnit + kTileRows - 1) / kTileRows;
     if (p.n_tiles_max > kMaxTiles) return false;
     // TMEM: per epilogue group `land` fp32 landing tiles (32 columns each) and
-    // `held` slabs of fp16 tiles (16 columns each); two landing tiles when that
-    // still leaves room for at least two held slabs.
-    const int slab_cols = p.n_tiles_max * 16;
+    // `held` slabs of its fp16 tiles (16 columns per tile, tiles_per_group tiles
+    // per slab); two landing tiles when that still leaves room for two held slabs.
+    p.tiles_per_group = (p.n_tiles_max + 1) / 2;
+    const int slab_cols = p.tiles_per_group * 16;
     p.land = 2;
     p.held = (kTmemCols / 2 - p.land * kRP) / slab_cols;
     if (p.held < 2) {
@@ -833,32 +897,39 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     p.scale = 1.0f / sqrtf((float)q.d);
     p.scale_log2e = p.scale * 1.4426950408889634f;
     const int stage_bytes = kTileRows * q.d * 2;
-    const int n_bars_max = 2 * 8 + 4 + 8 + 4 * kRing + 2;
-    const int c_bytes = 2 * p.held * p.n_tiles_max * kRP * 4;
-    const int fixed = 2 * kRP * q.d * 2                      // query images
-                      + 2 * kRP * 4 * 33 * 4                  // reduction buffers
-                      + 2 * p.n_tiles_max * p.N * kTileRows * 4   // running max (one per group)
-                      + c_bytes                               // fp16 references
-                      + kRing * kRP * 8 + kRing * kRP * 4 + 16
-                      + n_bars_max * 8 + 16 + 1024;
-    p.stages = std::min(6, (kSmemBudget - fixed) / stage_bytes);
+    const int q_bytes = kRP * q.d * 2;
+    const int n_bars = 2 * 8 + 2 * kMaxQ + 4 * kMaxLand + 2 * kStatsRing + 2 * kRing + 2;
+    const int w_bytes = 16 * 16 * 33 * 4;                   // transpose buffer per epilogue warp
+    const int acc_bytes = 2 * p.n_tiles_max * p.N * kTileRows * 4;   // running max (one per group)
+    const int c_bytes = 2 * p.held * p.tiles_per_group * 4 * kRP * 4;   // fp16 references per quadrant
+    const int ring_bytes = kStatsRing * 2 * 4 * kRP * 8 + kRing * kRP * 4;
+    const int fixed = w_bytes + acc_bytes + c_bytes + ring_bytes + 16 + n_bars * 8 + 16 + 1024;
+    // query images: the TMA loads slab s's image once slab s - nq is done, so
+    // with one or two tiles per slab a ring of four keeps it ahead of the K
+    // stream; with more tiles two are enough
+    p.nq = p.n_tiles_max <= 2 ? kMaxQ : 2;
+    p.stages = std::min(6, (kSmemBudget - fixed - p.nq * q_bytes) / stage_bytes);
+    if (p.stages < 3 && p.nq > 2) {
+        p.nq = 2;
+        p.stages = std::min(6, (kSmemBudget - fixed - p.nq * q_bytes) / stage_bytes);
+    }
     if (p.stages < 2) return false;
     int off = p.stages * stage_bytes;
     p.off_q = off;
-    off += 2 * kRP * q.d * 2;
+    off += p.nq * q_bytes;
     p.off_s = off;
-    off += 2 * kRP * 4 * 33 * 4;
+    off += w_bytes;
     p.off_acc = off;
-    off += 2 * p.n_tiles_max * p.N * kTileRows * 4;
+    off += acc_bytes;
     p.off_c = off;
     off += c_bytes;
     p.off_stats = off;
-    off += kRing * kRP * 8;
+    off += kStatsRing * 2 * 4 * kRP * 8;
     p.off_lse = off;
     off += kRing * kRP * 4;
     off = (off + 15) & ~15;
     p.off_bar = off;
-    off += (2 * p.stages + 4 + 8 + 4 * kRing + 2) * 8 + 16;
+    off += (2 * p.stages + 2 * kMaxQ + 4 * kMaxLand + 2 * kStatsRing + 2 * kRing + 2) * 8 + 16;
     // slack for 1024-byte alignment; more than half of the SM's shared memory, so
     // that one CTA runs per SM (each CTA allocates all 512 TMEM columns)
     p.smem_bytes = std::max(off + 1024, 116 * 1024);
@@ -966,14 +1037,9 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
         return SP_ECUDA;
     }
 
-    // zero the header, the tagged lse entries and the partial statistics this
-    // launch uses ([S][kRP][P] words)
-    SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
-    SP_CUDA_TRY(cudaMemsetAsync(w + plan.off_lse, 0,
-                                plan.off_partials - plan.off_lse + (size_t)p.S * kRP * p.P * 8, st));
     tc_prep_kernel<<<p.S, 256, 0, st>>>(p, static_cast<const __nv_bfloat16*>(q.Q),
                                         static_cast<const __nv_bfloat16*>(q.Kla), w + plan.off_qimg,
-                                        reinterpret_cast<float2*>(w + plan.off_la));
+                                        reinterpret_cast<float2*>(w + plan.off_la), p.lse, p.partials, p.hdr);
     SP_LAUNCH_CHECK();
 
     switch (q.d * 16 + p.G) {
