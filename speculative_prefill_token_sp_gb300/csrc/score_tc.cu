@@ -82,6 +82,8 @@ constexpr int kRing = 16;            // entries of the lse ring
 constexpr int kStatsRing = 4;        // entries of the statistics ring
 constexpr int kMaxQ = 4;             // query-image buffers
 constexpr int kMaxLand = 4;          // landing tiles per epilogue group
+constexpr int kMaxClasses = 8;       // slab classes, at most
+constexpr int kMinClassTokens = 384; // tokens per CTA per slab that need no further classes
 constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
@@ -90,6 +92,8 @@ struct TcParams {
     int L, H, H_kv, G, N, R, d;
     int S;              // slabs = L * H_kv
     int P;              // CTAs
+    int F;              // slab classes: CTA c takes slabs s = c % F, c % F + F, ...
+    int Pc;             // CTAs per class (P = F * Pc), one token range each
     int U;              // 32-token units of the prompt
     int n_tiles_max;
     int land;           // landing tiles per epilogue group
@@ -110,6 +114,8 @@ struct TcParams {
     unsigned long long* lse;        // [S][kRP] (lse bits, tag 1); 0 = not yet published
     WsHeader* hdr;
     float* importance;
+    unsigned* acc_glob;             // [N][T] order-preserving codes of the combined maxima (F > 1)
+    int* arrivals;                  // [Pc] CTAs of a range done with their maxima (F > 1)
 };
 
 // ---------------------------------------------------------------------------
@@ -313,6 +319,17 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Order-preserving 32-bit code of a float (a < b  <=>  code(a) < code(b) as
+// unsigned), so that atomicMax on codes takes the max of floats; 0 is below
+// the code of every float.
+__device__ __forceinline__ unsigned order_code(float x) {
+    const unsigned b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float order_decode(unsigned c) {
+    return __uint_as_float((c & 0x80000000u) ? (c ^ 0x80000000u) : ~c);
+}
+
 // Merge softmax statistics (m2, z2) into (m, z) (natural-log domain).
 __device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
     if (m2 == -INFINITY) return;
@@ -339,8 +356,16 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
     if (s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
     if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
     {
-        unsigned long long* ps = partials + (size_t)s * kRP * p.P;
-        for (int i = threadIdx.x; i < kRP * p.P; i += blockDim.x) ps[i] = 0ull;
+        unsigned long long* ps = partials + (size_t)s * kRP * p.Pc;
+        for (int i = threadIdx.x; i < kRP * p.Pc; i += blockDim.x) ps[i] = 0ull;
+    }
+    if (p.F > 1) {
+        // combined running maxima (0 is below every encoded float) and the
+        // per-range arrival counters
+        const size_t n = (size_t)p.N * p.T;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+            p.acc_glob[i] = 0u;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.Pc; i += gridDim.x * blockDim.x) p.arrivals[i] = 0;
     }
     const int cpr = p.d / 8;                      // 16-byte chunks per row
     uint8_t* img = qimg + (size_t)s * kRP * p.d * 2;
@@ -402,8 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
-    // this CTA's token range [t_begin, t_end) of every slab
-    const int u0 = (int)(((int64_t)c * p.U) / p.P), u1 = (int)(((int64_t)(c + 1) * p.U) / p.P);
+    // Slab class and token range of this CTA: it takes slabs s = cf, cf + F, ...
+    // (n_slabs of them) over the tokens [t_begin, t_end) of each.  The F CTAs
+    // with the same range combine their running maxima at the end.
+    const int cf = c % p.F, cr = c / p.F;
+    const int n_slabs = (p.S - cf + p.F - 1) / p.F;
+    const int u0 = (int)(((int64_t)cr * p.U) / p.Pc), u1 = (int)(((int64_t)(cr + 1) * p.U) / p.Pc);
     const int64_t t_begin = (int64_t)u0 * kUnit;
     const int64_t t_end = min((int64_t)u1 * kUnit, p.T);
     const int len = (int)(t_end - t_begin);
@@ -431,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     volatile uint32_t* tmem_base_sh = reinterpret_cast<volatile uint32_t*>(final_bar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
     volatile int* published = abort_flag + 1;      // slabs this CTA has published
+    volatile int* last_flag = published + 1;       // this CTA completes its token range (F > 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -479,9 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int s = 0; s < p.S && ok; ++s) {
-                const int qb = s % p.nq;
-                if (s >= p.nq) ok = mbar_wait(smem_u32(&q_empty[qb]), ((s / p.nq) - 1) & 1, abort_flag, p.hdr, 1);
+            for (int i = 0; i < n_slabs && ok; ++i) {
+                const int s = cf + i * p.F, qb = i % p.nq;
+                if (i >= p.nq) ok = mbar_wait(smem_u32(&q_empty[qb]), ((i / p.nq) - 1) & 1, abort_flag, p.hdr, 1);
                 if (!ok) break;
                 mbar_expect_tx(smem_u32(&q_full[qb]), kQBytes);
                 bulk_load(smem_u32(q_buf + qb * kQBytes), p.qimg + (size_t)s * kQBytes, kQBytes,
@@ -516,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             int it = 0;
             int lt0 = 0, lt1 = 0;          // landing tiles written so far for each epilogue group
             bool ok = true;
-            for (int s = 0; s < p.S && ok; ++s) {
-                const int qb = s % p.nq;
-                ok = mbar_wait(smem_u32(&q_full[qb]), (s / p.nq) & 1, abort_flag, p.hdr, 4);
+            for (int i = 0; i < n_slabs && ok; ++i) {
+                const int qb = i % p.nq;
+                ok = mbar_wait(smem_u32(&q_full[qb]), (i / p.nq) & 1, abort_flag, p.hdr, 4);
                 if (!ok) break;
                 const uint32_t qaddr = smem_u32(q_buf + qb * kQBytes);
                 for (int t = 0; t < n_tiles; ++t, ++it) {
@@ -576,9 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         const int odd = n_tiles & 1;
         int lt = 0;                                    // landing tiles consumed so far
         bool ok = true;
-        for (int i = 0; i < p.S + p.lag && ok; ++i) {
-            // ---- P1: statistics of slab i over this group's tiles, kept as fp16 offsets ----
-            if (i < p.S) {
+        for (int i = 0; i < n_slabs + p.lag && ok; ++i) {
+            // ---- P1: statistics of this CTA's i-th slab over the group's tiles, as fp16 offsets ----
+            if (i < n_slabs) {
                 const int s = i, q = s % kStatsRing, hs = s % p.held;
                 const int t0 = (grp + s * odd) & 1;    // this group's first tile of the slab
                 if (s >= kStatsRing &&
@@ -643,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&stats_full[q]));
             }
-            // ---- P2: normalise this group's tiles of slab i - lag, fold the max ----
+            // ---- P2: normalise the group's tiles of the (i - lag)-th slab, fold the max ----
             if (i >= p.lag) {
                 const int s = i - p.lag, q = s % kRing, hs = s % p.held;
                 const int t0 = (grp + s * odd) & 1;
@@ -683,17 +713,50 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             }
         }
         epi_sync();                                    // both groups' running maxima are complete
-        if (!*abort_flag && rh == 0) {
-            // importance of this CTA's tokens: (1/N) sum_j exp(max_{l,h}(s - lse))
-            const float inv_n = 1.0f / (float)p.N;
-            const size_t half = (size_t)p.n_tiles_max * p.N * kTileRows;
-            for (int t = grp; t < n_tiles; t += 2) {
-                const int k = t * kTileRows + tok;
-                if (k < len) {
-                    const float* a = acc + (size_t)t * p.N * kTileRows + tok;
-                    float sum = 0.f;
-                    for (int jj = 0; jj < p.N; ++jj) sum += expf(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows]));
-                    p.importance[t_begin + k] = sum * inv_n;
+        // importance of a token: (1/N) sum_j exp(max_{l,h}(s - lse))
+        const float inv_n = 1.0f / (float)p.N;
+        const size_t half = (size_t)p.n_tiles_max * p.N * kTileRows;
+        if (p.F == 1) {
+            if (!*abort_flag && rh == 0) {
+                for (int t = grp; t < n_tiles; t += 2) {
+                    const int k = t * kTileRows + tok;
+                    if (k < len) {
+                        const float* a = acc + (size_t)t * p.N * kTileRows + tok;
+                        float sum = 0.f;
+                        for (int jj = 0; jj < p.N; ++jj) sum += expf(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows]));
+                        p.importance[t_begin + k] = sum * inv_n;
+                    }
+                }
+            }
+        } else {
+            // fold this CTA's maxima (over its slab class) into the range's
+            // combined maxima; the last of the range's F CTAs to arrive turns
+            // them into importance
+            if (!*abort_flag) {
+                for (int t = grp; t < n_tiles; t += 2) {
+                    const int k = t * kTileRows + tok;
+                    if (k < len) {
+                        const float* a = acc + (size_t)t * p.N * kTileRows + tok;
+                        for (int jj = rh; jj < p.N; jj += 2)
+                            atomicMax(&p.acc_glob[(size_t)jj * p.T + t_begin + k],
+                                      order_code(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows])));
+                    }
+                }
+            }
+            __threadfence();
+            epi_sync();
+            if (ew == 0 && lane == 0) *last_flag = atomicAdd(&p.arrivals[cr], 1) == p.F - 1 ? 1 : 0;
+            epi_sync();
+            if (*last_flag && !*abort_flag && rh == 0) {
+                __threadfence();
+                for (int t = grp; t < n_tiles; t += 2) {
+                    const int k = t * kTileRows + tok;
+                    if (k < len) {
+                        float sum = 0.f;
+                        for (int jj = 0; jj < p.N; ++jj)
+                            sum += expf(order_decode(__ldcg(&p.acc_glob[(size_t)jj * p.T + t_begin + k])));
+                        p.importance[t_begin + k] = sum * inv_n;
+                    }
                 }
             }
         }
@@ -701,9 +764,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         // ------------------------------ publish ------------------------------
         // lane r merges row r's statistics over the two groups and four
         // quadrants and writes them to global memory as one 64-bit word.
-        for (int s = 0; s < p.S; ++s) {
-            const int q = s % kStatsRing;
-            if (!warp_wait(smem_u32(&stats_full[q]), (s / kStatsRing) & 1, abort_flag, p.hdr, 9)) break;
+        for (int i = 0; i < n_slabs; ++i) {
+            const int s = cf + i * p.F, q = i % kStatsRing;
+            if (!warp_wait(smem_u32(&stats_full[q]), (i / kStatsRing) & 1, abort_flag, p.hdr, 9)) break;
             float m = -INFINITY, z = 0.f;
 #pragma unroll
             for (int part = 0; part < 8; ++part) {
@@ -712,21 +775,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&stats_empty[q]));
-            st64(&p.partials[((size_t)s * kRP + lane) * p.P + c], pack2(m, z));
+            st64(&p.partials[((size_t)s * kRP + lane) * p.Pc + cr], pack2(m, z));
             __syncwarp();
-            if (lane == 0) *published = s + 1;      // wakes this CTA's merge warps for slab s if it is theirs
+            if (lane == 0) *published = i + 1;      // wakes this CTA's merge warps for slab s if it is theirs
         }
     } else if (warp < kFetchWarp) {
         // ------------------------------ merge ------------------------------
-        // Slab s is merged by CTA s mod P, once this CTA has published its own
-        // statistics of s (the other CTAs are then a few microseconds from done):
-        // the entries are read until every CTA's is there.
+        // The class's i-th slab is merged by its CTA with range i mod Pc, once
+        // that CTA has published its own statistics of it (the other CTAs are then
+        // a few microseconds from done): the entries are read until all are there.
         const int mi = threadIdx.x - kMergeBase;       // 0..127
         const int r = mi >> 2, part = mi & 3;
-        for (int s = c; s < p.S; s += p.P) {
+        for (int i = cr; i < n_slabs; i += p.Pc) {
+            const int s = cf + i * p.F;
             if (mi == 0) {
                 const unsigned long long t0 = global_ns();
-                while (*published <= s) {
+                while (*published <= i) {
                     if (*abort_flag) break;
                     if (global_ns() - t0 > kTimeoutNs) {
                         record_error(p.hdr, SP_ETIMEOUT, 12);
@@ -737,17 +801,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 }
             }
             if (merge_sync_any(*abort_flag != 0)) break;
-            const unsigned long long* src = p.partials + ((size_t)s * kRP + r) * p.P;
+            const unsigned long long* src = p.partials + ((size_t)s * kRP + r) * p.Pc;
             const float2 la = __ldcg(&p.la[(size_t)s * kRP + r]);
             float m = -INFINITY, z = 0.f;
             bool ok = true;
-            for (int base = part; base < p.P && ok; base += 64) {
+            for (int base = part; base < p.Pc && ok; base += 64) {
                 // all loads of the batch first (up to 16 in flight per thread)
                 unsigned long long v[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int cc = base + 4 * k;
-                    v[k] = cc < p.P ? ld_cg64(src + cc) : 0ull;
+                    v[k] = cc < p.Pc ? ld_cg64(src + cc) : 0ull;
                 }
                 // an entry whose store is not visible yet reads as 0: read the missing
                 // ones again, all in flight together
@@ -756,22 +820,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     bool missing = false;
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        if (base + 4 * k < p.P && (v[k] >> 32) == 0ull) missing = true;
+                        if (base + 4 * k < p.Pc && (v[k] >> 32) == 0ull) missing = true;
                     if (!missing) break;
                     if (*abort_flag || global_ns() - t0 > kTimeoutNs) { ok = false; break; }
                     __nanosleep(64);
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        if (base + 4 * k < p.P && (v[k] >> 32) == 0ull) v[k] = ld_cg64(src + base + 4 * k);
+                        if (base + 4 * k < p.Pc && (v[k] >> 32) == 0ull) v[k] = ld_cg64(src + base + 4 * k);
                 }
                 float mb = -INFINITY;
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    if (base + 4 * k < p.P) mb = fmaxf(mb, unpack2(v[k]).x);
+                    if (base + 4 * k < p.Pc) mb = fmaxf(mb, unpack2(v[k]).x);
                 float zb = 0.f;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    if (base + 4 * k >= p.P) continue;
+                    if (base + 4 * k >= p.Pc) continue;
                     const float2 f = unpack2(v[k]);
                     zb += f.y * __expf(f.x - mb);
                 }
@@ -796,10 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         }
     } else {
         // ------------------------------ fetch ------------------------------
-        for (int s = 0; s < p.S; ++s) {
-            const int q = s % kRing;
+        for (int i = 0; i < n_slabs; ++i) {
+            const int s = cf + i * p.F, q = i % kRing;
             bool ok = true;
-            if (lane == 0 && s >= kRing) ok = mbar_wait(smem_u32(&lse_empty[q]), ((s / kRing) - 1) & 1, abort_flag, p.hdr, 10);
+            if (lane == 0 && i >= kRing) ok = mbar_wait(smem_u32(&lse_empty[q]), ((i / kRing) - 1) & 1, abort_flag, p.hdr, 10);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             __syncwarp();
             if (!ok) break;
@@ -842,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
 struct Plan {
     TcParams p;
-    size_t off_qimg, off_la, off_partials, off_lse, total;
+    size_t off_qimg, off_la, off_partials, off_lse, off_acc_glob, off_arrivals, total;
 };
 
 int sm_count_or(int fallback) {
@@ -874,8 +938,18 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     p.S = q.L * q.H_kv;
     p.T = q.T;
     p.U = (int)((q.T + kUnit - 1) / kUnit);
-    p.P = std::max(1, std::min(std::min(P_hint, p.U), kMaxCtas));
-    const int units_max = (p.U + p.P - 1) / p.P;
+    const int P0 = std::max(1, std::min(std::min(P_hint, p.U), kMaxCtas));
+    // Slab classes: while a CTA would get fewer than kMinClassTokens tokens of
+    // each slab, halve the CTAs per slab (and double the tokens each gets).
+    // Per-slab costs (statistics exchange, hand-offs) then spread over more
+    // tokens; the F CTAs of a token range merge their maxima at the end.
+    p.F = 1;
+    while (p.F < kMaxClasses && p.S >= 2 * p.F && P0 / (2 * p.F) >= 1 &&
+           ((p.U + P0 / p.F - 1) / (P0 / p.F)) * kUnit < kMinClassTokens)
+        p.F *= 2;
+    p.Pc = P0 / p.F;
+    p.P = p.Pc * p.F;
+    const int units_max = (p.U + p.Pc - 1) / p.Pc;
     p.n_tiles_max = (units_max * kUnit + kTileRows - 1) / kTileRows;
     if (p.n_tiles_max > kMaxTiles) return false;
     // TMEM: per epilogue group `land` fp32 landing tiles (32 columns each) and
@@ -941,6 +1015,8 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     out.off_la = cv.take(S * kRP * sizeof(float2));
     out.off_lse = cv.take(S * kRP * 8);                    // lse and partials are zeroed per call
     out.off_partials = cv.take(S * kRP * (size_t)kMaxCtas * 8);
+    out.off_acc_glob = cv.take((size_t)q.N * (size_t)q.T * 4);
+    out.off_arrivals = cv.take((size_t)kMaxCtas * 4);
     out.total = cv.off;
     return true;
 }
@@ -1022,6 +1098,8 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     p.partials = reinterpret_cast<unsigned long long*>(w + plan.off_partials);
     p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
     p.importance = q.importance;
+    p.acc_glob = reinterpret_cast<unsigned*>(w + plan.off_acc_glob);
+    p.arrivals = reinterpret_cast<int*>(w + plan.off_arrivals);
 
     // K viewed as a 2D tensor of L*H_kv*T rows by d bf16 columns; 32-row x 64-column boxes.
     CUtensorMap map;
