@@ -83,7 +83,7 @@ constexpr int kStatsRing = 4;        // entries of the statistics ring
 constexpr int kMaxQ = 4;             // query-image buffers
 constexpr int kMaxLand = 4;          // landing tiles per epilogue group
 constexpr int kMaxClasses = 8;       // slab classes, at most
-constexpr int kMinClassTokens = 384; // tokens per CTA per slab that need no further classes
+constexpr int kMinClassTokens = 768; // tokens per CTA per slab that need no further classes
 constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
@@ -940,12 +940,14 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     p.U = (int)((q.T + kUnit - 1) / kUnit);
     const int P0 = std::max(1, std::min(std::min(P_hint, p.U), kMaxCtas));
     // Slab classes: while a CTA would get fewer than kMinClassTokens tokens of
-    // each slab, halve the CTAs per slab (and double the tokens each gets).
-    // Per-slab costs (statistics exchange, hand-offs) then spread over more
-    // tokens; the F CTAs of a token range merge their maxima at the end.
+    // each slab, halve the CTAs per slab (and double the tokens each gets, up
+    // to kMaxTiles tiles).  Per-slab costs (statistics exchange, hand-offs,
+    // part-filled tiles) then spread over more tokens; the F CTAs of a token
+    // range merge their maxima at the end.
+    auto units_per_cta = [&](int F) { return (p.U + P0 / F - 1) / (P0 / F); };
     p.F = 1;
     while (p.F < kMaxClasses && p.S >= 2 * p.F && P0 / (2 * p.F) >= 1 &&
-           ((p.U + P0 / p.F - 1) / (P0 / p.F)) * kUnit < kMinClassTokens)
+           units_per_cta(p.F) * kUnit < kMinClassTokens && units_per_cta(2 * p.F) * kUnit <= kMaxTiles * kTileRows)
         p.F *= 2;
     p.Pc = P0 / p.F;
     p.P = p.Pc * p.F;
