@@ -62,6 +62,14 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def replica_throughput(world: int, tokens_per_replica: int, steps: int, local_total_ms: float):
+    """Whole-job throughput of `world` independent replicas: every rank scores
+    `tokens_per_replica` tokens per step, and the job takes as long as its
+    slowest rank.  Returns (tokens per second, max-over-ranks total ms)."""
+    total_ms = max_over_ranks(local_total_ms, world)
+    return world * tokens_per_replica * steps / (total_ms / 1e3), total_ms
+
+
 def barrier(world: int) -> None:
     if world > 1:
         import torch.distributed as dist
@@ -343,9 +351,8 @@ def run_gpu(args) -> None:
             torch.cuda.synchronize()
     launches = sp.sp_kernel_launches() - launches0
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = max_over_ranks(sum(step_ms), world)
+    value, total_ms = replica_throughput(world, M, args.steps, sum(step_ms))
     ms_per_step = total_ms / args.steps
-    value = world * M * args.steps / (total_ms / 1e3)
     timed_launches = launches - 0  # includes the clock-tail steps; recount below
     per_step_launches = None
 
