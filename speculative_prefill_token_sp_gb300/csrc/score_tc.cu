@@ -103,7 +103,10 @@ struct TcParams {
     int held_base;      // first TMEM column of the held regions
     int stages;
     int nq;             // query-image buffers (2 or 4)
-    int64_t T;          // rows per slab in K (= M for one prompt)
+    int64_t T;          // tokens of the prompt (M)
+    int64_t slab_stride;  // rows between consecutive slabs in K (the packed token count)
+    int64_t tok0;       // row of the prompt's first token within a slab (its offset in the pack)
+    int first;          // 1 for the call's first prompt: its preparation clears the status
     float scale, scale_log2e;
     // shared-memory carve (byte offsets from the 1024-aligned base)
     int off_q, off_s, off_acc, off_c, off_stats, off_lse, off_bar, smem_bytes;
@@ -358,7 +361,8 @@ __device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
 // ---------------------------------------------------------------------------
 // Per-call preparation (one block per slab): the swizzled query image, the
 // softmax statistics of the look-ahead keys, and the zeroed exchange entries
-// (a zero word means "not published yet"); block 0 also clears the status.
+// (a zero word means "not published yet"); block 0 of the call's first prompt
+// also clears the status.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __nv_bfloat16* __restrict__ Q,
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
     const int s = blockIdx.x;
     const int l = s / p.H_kv, g = s % p.H_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
+    if (p.first && s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
     if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
     {
         unsigned long long* ps = partials + (size_t)s * kRP * p.Pc;
@@ -532,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 mbar_expect_tx(smem_u32(&q_full[qb]), kQBytes);
                 bulk_load(smem_u32(q_buf + qb * kQBytes), p.qimg + (size_t)s * kQBytes, kQBytes,
                           smem_u32(&q_full[qb]));
-                const int64_t row0 = (int64_t)s * p.T + t_begin;
+                const int64_t row0 = (int64_t)s * p.slab_stride + p.tok0 + t_begin;
                 for (int t = 0; t < n_tiles; ++t, ++it) {
                     const int st = it % p.stages;
                     if (it >= p.stages)
@@ -938,7 +942,7 @@ int sm_count_or(int fallback) {
 }
 
 bool shape_ok(const ScoreProblem& q) {
-    if (q.dtype != SP_BF16 || q.B != 1 || q.N < 1) return false;
+    if (q.dtype != SP_BF16 || q.B < 1 || q.N < 1 || q.max_M < 1) return false;
     if (q.d != 64 && q.d != 128) return false;
     const int G = q.H / q.H_kv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return false;
@@ -948,14 +952,17 @@ bool shape_ok(const ScoreProblem& q) {
     return true;
 }
 
-// Plan for P CTAs; returns false if the problem does not fit this path.
-bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
-    if (!shape_ok(q)) return false;
+// Plan for one prompt of M tokens of the problem's shape on up to P_hint CTAs;
+// returns false if it does not fit this path.
+bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
+    if (!shape_ok(q) || M < 1 || M > q.max_M) return false;
     TcParams& p = out.p;
     p.L = q.L; p.H = q.H; p.H_kv = q.H_kv; p.G = q.H / q.H_kv; p.N = q.N; p.R = q.N * p.G; p.d = q.d;
     p.S = q.L * q.H_kv;
-    p.T = q.T;
-    p.U = (int)((q.T + kUnit - 1) / kUnit);
+    p.T = M;
+    p.slab_stride = q.T;
+    p.tok0 = 0;
+    p.U = (int)((M + kUnit - 1) / kUnit);
     const int P0 = std::max(1, std::min(std::min(P_hint, p.U), kMaxCtas));
     // Slab classes: while a CTA would get fewer than kMinClassTokens tokens of
     // each slab, halve the CTAs per slab (and double the tokens each gets, up
@@ -1035,7 +1042,7 @@ bool make_plan(const ScoreProblem& q, int P_hint, Plan& out) {
     out.off_la = cv.take(S * kRP * sizeof(float2));
     out.off_lse = cv.take(S * kRP * 8);                    // lse and partials are zeroed per call
     out.off_partials = cv.take(S * kRP * (size_t)kMaxCtas * 8);
-    out.off_acc_glob = cv.take((size_t)q.N * (size_t)q.T * 4);
+    out.off_acc_glob = cv.take((size_t)q.N * (size_t)M * 4);
     out.off_arrivals = cv.take((size_t)kMaxCtas * 4);
     out.total = cv.off;
     return true;
@@ -1090,56 +1097,41 @@ sp_status launch_kernel(const CUtensorMap& map, const TcParams& p, cudaStream_t 
 
 bool score_tc_supported(const ScoreProblem& q) {
     Plan plan;
-    return make_plan(q, sm_count_or(148), plan);
+    return make_plan(q, q.max_M, sm_count_or(148), plan);
 }
 
 size_t score_tc_ws_bytes(const ScoreProblem& q) {
+    // the workspace is reused prompt after prompt; the largest prompt needs the most
     Plan plan;
-    return make_plan(q, kMaxCtas, plan) ? plan.total : 0;
+    return make_plan(q, q.max_M, kMaxCtas, plan) ? plan.total : 0;
 }
 
-sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
+// One prompt (b) of a packed batch: its plan, workspace pointers and launches.
+static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const CUtensorMap& map, int sms,
+                               void* ws, cudaStream_t st) {
+    const int64_t M = q.cu_M_host[b + 1] - q.cu_M_host[b];
     Plan plan;
-    const int sms = sm_count_or(0);
-    if (sms < 1 || !make_plan(q, sms, plan)) {
-        set_error("sp_score: shape outside the tensor-core path");
+    if (!make_plan(q, M, sms, plan)) {
+        set_error("sp_score: prompt %d (%lld tokens) is outside the tensor-core path", b, (long long)M);
         return SP_EUNSUPPORTED;
     }
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) {
-        set_error("sp_score: cuTensorMapEncodeTiled is unavailable from the driver");
-        return SP_ECUDA;
-    }
     TcParams& p = plan.p;
+    p.tok0 = q.cu_M_host[b];
+    p.first = first ? 1 : 0;
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.hdr = reinterpret_cast<WsHeader*>(w);
     p.qimg = w + plan.off_qimg;
     p.la = reinterpret_cast<const float2*>(w + plan.off_la);
     p.partials = reinterpret_cast<unsigned long long*>(w + plan.off_partials);
     p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
-    p.importance = q.importance;
+    p.importance = q.importance + q.cu_M_host[b];
     p.acc_glob = reinterpret_cast<unsigned*>(w + plan.off_acc_glob);
     p.arrivals = reinterpret_cast<int*>(w + plan.off_arrivals);
-
-    // K viewed as a 2D tensor of L*H_kv*T rows by d bf16 columns; 32-row x 64-column boxes.
-    CUtensorMap map;
-    const cuuint64_t gdim[2] = {(cuuint64_t)q.d, (cuuint64_t)p.S * (cuuint64_t)q.T};
-    const cuuint64_t gstride[1] = {(cuuint64_t)q.d * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)kBoxRows};
-    const cuuint32_t estride[2] = {1u, 1u};
-    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q.K), gdim, gstride, box,
-                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) {
-        set_error("sp_score: cuTensorMapEncodeTiled failed (%d)", (int)cr);
-        return SP_ECUDA;
-    }
-
-    tc_prep_kernel<<<p.S, 256, 0, st>>>(p, static_cast<const __nv_bfloat16*>(q.Q),
-                                        static_cast<const __nv_bfloat16*>(q.Kla), w + plan.off_qimg,
-                                        reinterpret_cast<float2*>(w + plan.off_la), p.lse, p.partials, p.hdr);
+    const __nv_bfloat16* Qb = static_cast<const __nv_bfloat16*>(q.Q) + (size_t)b * q.N * q.L * q.H * q.d;
+    const __nv_bfloat16* Klab = static_cast<const __nv_bfloat16*>(q.Kla) + (size_t)b * q.L * q.H_kv * q.N * q.d;
+    tc_prep_kernel<<<p.S, 256, 0, st>>>(p, Qb, Klab, w + plan.off_qimg, reinterpret_cast<float2*>(w + plan.off_la),
+                                        p.lse, p.partials, p.hdr);
     SP_LAUNCH_CHECK();
-
     switch (q.d * 16 + p.G) {
         case 64 * 16 + 1: return launch_kernel<64, 1>(map, p, st);
         case 64 * 16 + 2: return launch_kernel<64, 2>(map, p, st);
@@ -1153,6 +1145,45 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     }
     set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, p.G);
     return SP_EUNSUPPORTED;
+}
+
+sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
+    const int sms = sm_count_or(0);
+    if (sms < 1 || !shape_ok(q)) {
+        set_error("sp_score: shape outside the tensor-core path");
+        return SP_EUNSUPPORTED;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) {
+        set_error("sp_score: cuTensorMapEncodeTiled is unavailable from the driver");
+        return SP_ECUDA;
+    }
+    const int S = q.L * q.H_kv;
+    // K viewed as a 2D tensor of L*H_kv*T rows (T: the packed tokens) by d bf16 columns;
+    // 32-row x 64-column boxes.
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)q.d, (cuuint64_t)S * (cuuint64_t)q.T};
+    const cuuint64_t gstride[1] = {(cuuint64_t)q.d * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kBoxRows};
+    const cuuint32_t estride[2] = {1u, 1u};
+    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q.K), gdim, gstride, box,
+                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        set_error("sp_score: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+        return SP_ECUDA;
+    }
+
+    // one prompt after another, each with its own plan; they share the workspace
+    // (stream order separates them)
+    bool first = true;
+    for (int b = 0; b < q.B; ++b) {
+        if (q.cu_M_host[b + 1] == q.cu_M_host[b]) continue;
+        const sp_status s = launch_prompt(q, b, first, map, sms, ws, st);
+        if (s != SP_OK) return s;
+        first = false;
+    }
+    return SP_OK;
 }
 
 }  // namespace sp
