@@ -34,7 +34,7 @@ pinned by the tests only as far as the mathematics allows):
   * N = 0 look-ahead steps gives importance 1.0 everywhere (the guide's
     compute_imp fallback when nothing was captured).
 """
-from .score import importance, attention_rows, lookahead_rows  # noqa: F401
+from .score import importance, attention_rows, lookahead_rows, row_lse, importance_given_lse  # noqa: F401
 from .select import (  # noqa: F401
     chunk_sums, chunk_means, avg_pool, keep_count, topk_chunks, normalize_boost,
     mass_chunks, kept_positions, select, select_varlen,

@@ -100,3 +100,56 @@ def importance(Q_la, K_prompt, K_la) -> np.ndarray:
     for j in range(N):                              # mean over look-ahead steps, j in order
         total += best[j]
     return total / N
+
+
+def row_lse(Q_la, K_prompt, K_la) -> np.ndarray:
+    """lse[l, h, j] = log(sum_i exp(s[l,h,j,i]) + sum_{k<=j} exp(u[l,h,j,k]))  (fp64, [L, H, N]).
+
+    The normaliser of look-ahead query j's softmax over the M prompt keys and
+    look-ahead keys 0..j: the quantity the speculator's own look-ahead decode
+    attention already holds.  Computed with the max shift, row by row.
+    """
+    N, L, H, d = Q_la.shape
+    H_kv = K_prompt.shape[1]
+    G = H // H_kv
+    out = np.empty((L, H, N), dtype=np.float64)
+    for l in range(L):
+        for g in range(H_kv):
+            k = _f64(K_prompt[l, g])
+            for h in range(g * G, (g + 1) * G):
+                q = _f64(Q_la[:, l, h, :])
+                s = (q @ k.T) / math.sqrt(d)
+                u = lookahead_rows(Q_la, K_la, l, h, G)
+                for j in range(N):
+                    row = np.concatenate([s[j], u[j, :j + 1]])
+                    m = row.max()
+                    out[l, h, j] = m + math.log(np.exp(row - m).sum())
+    return out
+
+
+def importance_given_lse(Q_la, K_prompt, lse) -> np.ndarray:
+    """importance_i = (1/N) sum_j max_{l,h} exp(s[l,h,j,i] - lse[l,h,j])  (fp64, [M]).
+
+    The same max/max/mean aggregation as importance(), with each row's softmax
+    normaliser lse[L, H, N] given by the caller instead of computed from the
+    keys (the single-pass variant: K is read once).
+    """
+    N, L, H, d = Q_la.shape
+    H_kv, M = K_prompt.shape[1], K_prompt.shape[2]
+    G = H // H_kv
+    lse = np.asarray(lse, dtype=np.float64)
+    if N == 0:
+        return np.ones(M, dtype=np.float64)
+    best = np.zeros((N, M), dtype=np.float64)
+    for l in range(L):
+        for g in range(H_kv):
+            k = _f64(K_prompt[l, g])
+            for h in range(g * G, (g + 1) * G):
+                q = _f64(Q_la[:, l, h, :])
+                s = (q @ k.T) / math.sqrt(d)        # [N, M]
+                a = np.exp(s - lse[l, h][:, None])
+                np.maximum(best, a, out=best)
+    total = np.zeros(M, dtype=np.float64)
+    for j in range(N):
+        total += best[j]
+    return total / N
