@@ -109,6 +109,33 @@ sp_status sp_score(const void* Q_la, const void* K_prompt, const void* K_la,
                    int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype,
                    float* importance, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes sp_score_lse needs for this shape (0 if the shape is invalid). */
+size_t sp_score_lse_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype);
+
+/* Token importance of one prompt when each row's softmax normaliser is
+ * already known (single pass: K is read once, no statistics pass).
+ *
+ * Defines: importance[i] = (1/N) sum_j max_{l,h} exp(Q_la[j,l,h,:] . K[l,g,i,:] / sqrt(d)
+ * - lse[l,h,j]), g = h / (H / H_kv) -- the aggregation of sp_score (paper
+ * review, "core formulas"; llama.cpp guide, "Token Importance"), with lse
+ * supplied by the caller.  With lse[l,h,j] the log of the sum of exp over
+ * the M prompt logits and the look-ahead logits 0..j -- the normaliser the
+ * speculator's own look-ahead decode attention computes -- the result equals
+ * sp_score's.  The pages have no separate call for this; it is the
+ * "lse-in" variant of the same definition.
+ *
+ *   Q_la      [N, L, H, d]      look-ahead queries (post-RoPE), dtype
+ *   K_prompt  [L, H_kv, M, d]   prompt keys (post-RoPE), dtype
+ *   lse       [L, H, N]         fp32 natural-log normalisers (device memory, 4-byte aligned)
+ *   importance[M]               fp32 output
+ *
+ * Requirements and errors as sp_score; N == 0 writes 1.0 and reads no lse.
+ * Accuracy: within 1e-3 absolute and 1e-2 relative of an fp64 evaluation on
+ * the same inputs (bf16), 1e-5 (fp32). */
+sp_status sp_score_lse(const void* Q_la, const void* K_prompt, const float* lse,
+                       int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype,
+                       float* importance, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes for sp_score_varlen (cu_M_host: B+1 host prefix sums). */
 size_t sp_score_varlen_workspace_size(int B, const int64_t* cu_M_host, int L, int H, int H_kv,
                                       int d, int N, sp_dtype dtype);

@@ -108,6 +108,8 @@ ScoreProblem make_score_problem(const void* Q, const void* K, const void* Kla, i
                                 int L, int H, int H_kv, int d, int N, sp_dtype dtype, float* imp) {
     ScoreProblem p;
     p.Q = Q; p.K = K; p.Kla = Kla; p.importance = imp; p.cu_M_host = cu;
+    p.lse_in = nullptr;
+    p.lse_mode = false;
     p.B = B; p.L = L; p.H = H; p.H_kv = H_kv; p.d = d; p.N = N; p.dtype = dtype;
     p.T = cu[B];
     p.max_M = 0;
@@ -124,12 +126,14 @@ size_t score_ws(const ScoreProblem& p) {
 sp_status run_score(const char* fn, const ScoreProblem& p, void* ws, size_t ws_bytes, void* stream) {
     const size_t need = score_ws(p);
     if (p.T > 0 && p.N > 0) {
-        if (!p.Q || !p.K || !p.Kla) {
+        const void* third = p.lse_mode ? static_cast<const void*>(p.lse_in) : p.Kla;
+        if (!p.Q || !p.K || !third) {
             set_error("%s: null input pointer", fn);
             return SP_EINVAL;
         }
-        if (!aligned16(p.Q) || !aligned16(p.K) || !aligned16(p.Kla)) {
-            set_error("%s: input pointers must be 16-byte aligned", fn);
+        if (!aligned16(p.Q) || !aligned16(p.K) || (!p.lse_mode && !aligned16(p.Kla)) ||
+            (p.lse_mode && reinterpret_cast<uintptr_t>(p.lse_in) % 4 != 0)) {
+            set_error("%s: input pointers must be 16-byte aligned (lse: 4-byte)", fn);
             return SP_EINVAL;
         }
     }
@@ -272,6 +276,30 @@ sp_status sp_score(const void* Q_la, const void* K_prompt, const void* K_la, int
     int64_t cu[2] = {0, M};
     ScoreProblem p = make_score_problem(Q_la, K_prompt, K_la, 1, cu, L, H, H_kv, d, N, dtype, importance);
     return run_score("sp_score", p, ws, ws_bytes, stream);
+}
+
+size_t sp_score_lse_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype) {
+    if (M < 0 || check_shape("sp_score_lse_workspace_size", L, H, H_kv, d, N, dtype) != SP_OK) return 0;
+    int64_t cu[2] = {0, M};
+    ScoreProblem p = make_score_problem(nullptr, nullptr, nullptr, 1, cu, L, H, H_kv, d, N, dtype, nullptr);
+    p.lse_mode = true;                  // the plan depends only on the mode
+    return score_ws(p);
+}
+
+sp_status sp_score_lse(const void* Q_la, const void* K_prompt, const float* lse, int L, int H, int H_kv,
+                       int d, int64_t M, int N, sp_dtype dtype, float* importance, void* ws,
+                       size_t ws_bytes, void* stream) {
+    sp_status s = check_shape("sp_score_lse", L, H, H_kv, d, N, dtype);
+    if (s != SP_OK) return s;
+    if (M < 0 || M > (int64_t)INT32_MAX) {
+        set_error("sp_score_lse: M must be in [0, 2^31-1] (got %lld)", (long long)M);
+        return M < 0 ? SP_EINVAL : SP_EUNSUPPORTED;
+    }
+    int64_t cu[2] = {0, M};
+    ScoreProblem p = make_score_problem(Q_la, K_prompt, nullptr, 1, cu, L, H, H_kv, d, N, dtype, importance);
+    p.lse_in = lse;
+    p.lse_mode = true;
+    return run_score("sp_score_lse", p, ws, ws_bytes, stream);
 }
 
 size_t sp_score_varlen_workspace_size(int B, const int64_t* cu_M_host, int L, int H, int H_kv, int d,

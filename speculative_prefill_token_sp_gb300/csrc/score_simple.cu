@@ -193,6 +193,19 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Geo geo, const 
     }
 }
 
+// (2') lse given by the caller (one prompt): lse_in[l, h, j] into this path's
+// [slab, row] layout, row r = j*G + h % G of slab l*H_kv + h / G.
+__global__ void lse_in_kernel(const Geo geo, const float* __restrict__ lse_in, float* __restrict__ lse) {
+    const int64_t n = (int64_t)geo.L * geo.H_kv * geo.R;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t sl = i / geo.R;
+        const int r = (int)(i % geo.R);
+        const int l = (int)(sl / geo.H_kv), g = (int)(sl % geo.H_kv);
+        const int j = r / geo.G, h = g * geo.G + r % geo.G;
+        lse[i] = lse_in[((int64_t)l * geo.H + h) * geo.N + j];
+    }
+}
+
 // (3) normalised weights, max over the heads of the group, atomicMax across
 // KV heads and layers.  Weights are >= 0, so their IEEE bits order like
 // unsigned integers.
@@ -311,10 +324,16 @@ sp_status launch_typed(const ScoreProblem& p, const Geo& geo, const Layout& lo, 
     SP_CUDA_TRY(cudaFuncSetAttribute(normmax_kernel<In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)sm_norm));
     dim3 grid(geo.max_splits, slabs * geo.n_rb);
-    stats_kernel<In><<<grid, kThreads, sm_stats, st>>>(geo, Q, K, partials);
-    SP_LAUNCH_CHECK();
-    combine_kernel<In><<<slabs, kThreads, 0, st>>>(geo, Q, Kla, partials, lse);
-    SP_LAUNCH_CHECK();
+    if (p.lse_mode) {
+        const int64_t n = (int64_t)slabs * geo.R;
+        lse_in_kernel<<<(int)std::min<int64_t>((n + 255) / 256, 1024), 256, 0, st>>>(geo, p.lse_in, lse);
+        SP_LAUNCH_CHECK();
+    } else {
+        stats_kernel<In><<<grid, kThreads, sm_stats, st>>>(geo, Q, K, partials);
+        SP_LAUNCH_CHECK();
+        combine_kernel<In><<<slabs, kThreads, 0, st>>>(geo, Q, Kla, partials, lse);
+        SP_LAUNCH_CHECK();
+    }
     normmax_kernel<In><<<grid, kThreads, sm_norm, st>>>(geo, Q, K, lse, acc);
     SP_LAUNCH_CHECK();
     int blocks = (int)std::min<int64_t>((geo.T + 255) / 256, 4096);

@@ -107,6 +107,8 @@ struct TcParams {
     int64_t slab_stride;  // rows between consecutive slabs in K (the packed token count)
     int64_t tok0;       // row of the prompt's first token within a slab (its offset in the pack)
     int first;          // 1 for the call's first prompt: its preparation clears the status
+    int lse_mode;       // 1: each row's lse is given (lse_in); no statistics pass, no exchange
+    const float* lse_in;  // [L, H, N] natural-log softmax normalisers (lse_mode)
     float scale, scale_log2e;
     // shared-memory carve (byte offsets from the 1024-aligned base)
     int off_q, off_s, off_acc, off_c, off_stats, off_lse, off_bar, smem_bytes;
@@ -374,8 +376,16 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
     const int l = s / p.H_kv, g = s % p.H_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (p.first && s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
-    if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
-    {
+    if (p.lse_mode) {
+        // the given lse, already published (tag 1) for the fetch warp; padded rows 0
+        if (threadIdx.x < kRP) {
+            const int r = threadIdx.x;
+            float v = 0.f;
+            if (r < p.R) v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N + r / p.G];
+            lse[(size_t)s * kRP + r] = (unsigned long long)__float_as_uint(v) | (1ull << 32);
+        }
+    } else {
+        if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
         unsigned long long* ps = partials + (size_t)s * kRP * p.Pc;
         for (int i = threadIdx.x; i < kRP * p.Pc; i += blockDim.x) ps[i] = 0ull;
     }
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
     }
     // row r (query j = r / G, head g*G + r % G) against look-ahead keys k <= j:
     // one warp per row, lanes split the dot product
-    for (int r = warp; r < kRP; r += blockDim.x / 32) {
+    for (int r = warp; r < kRP && !p.lse_mode; r += blockDim.x / 32) {
         float m = -INFINITY, z = 0.f;
         if (r < p.R) {
             const int j = r / p.G, h = g * p.G + r % p.G;
@@ -626,7 +636,46 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         const int odd = n_tiles & 1;
         int lt = 0;                                    // landing tiles consumed so far
         bool ok = true;
-        for (int i = 0; i < n_slabs + p.lag && ok; ++i) {
+        if (p.lse_mode) {
+            // lse given: one pass, exp(s - lse) straight from the landing tiles
+            for (int i = 0; i < n_slabs && ok; ++i) {
+                const int q = i % kRing, t0 = (grp + i * odd) & 1;
+                if (!warp_wait(smem_u32(&lse_full[q]), (i / kRing) & 1, abort_flag, p.hdr, 8)) {
+                    ok = false;
+                    break;
+                }
+                float lr[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) lr[r] = lse_ring[q * kRP + rh * 16 + r];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&lse_empty[q]));
+                for (int t = t0; t < n_tiles; t += 2, ++lt) {
+                    const int slot = grp * p.land + lt % p.land;
+                    if (!warp_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float x[16];
+                    tmem_ld16f(tmem_base + lane_addr + (uint32_t)(slot * kRP + rh * 16), x);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));
+                    float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
+#pragma unroll
+                    for (int jl = 0; jl < 16 / G; ++jl) {
+                        const int jj = rh * (16 / G) + jl;
+                        if (jj < p.N) {
+                            float m = fmaf(x[jl * G], p.scale, -lr[jl * G]);
+#pragma unroll
+                            for (int hh = 1; hh < G; ++hh) m = fmaxf(m, fmaf(x[jl * G + hh], p.scale, -lr[jl * G + hh]));
+                            a[jj * kTileRows] = fmaxf(a[jj * kTileRows], m);
+                        }
+                    }
+                }
+            }
+        }
+        for (int i = 0; i < (p.lse_mode ? 0 : n_slabs + p.lag) && ok; ++i) {
             // ---- P1: statistics of this CTA's i-th slab over the group's tiles, as fp16 offsets ----
             if (i < n_slabs) {
                 const int s = i, q = s % kStatsRing, hs = s % p.held;
@@ -786,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         // ------------------------------ publish ------------------------------
         // lane r merges row r's statistics over the two groups and four
         // quadrants and writes them to global memory as one 64-bit word.
-        for (int i = 0; i < n_slabs; ++i) {
+        for (int i = 0; i < (p.lse_mode ? 0 : n_slabs); ++i) {
             const int s = cf + i * p.F, q = i % kStatsRing;
             if (!warp_wait(smem_u32(&stats_full[q]), (i / kStatsRing) & 1, abort_flag, p.hdr, 9)) break;
             float m = -INFINITY, z = 0.f;
@@ -808,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         // a few microseconds from done): the entries are read until all are there.
         const int mi = threadIdx.x - kMergeBase;       // 0..127
         const int r = mi >> 2, part = mi & 3;
-        for (int i = cr; i < n_slabs; i += p.Pc) {
+        for (int i = cr; i < (p.lse_mode ? 0 : n_slabs); i += p.Pc) {
             const int s = cf + i * p.F;
             if (mi == 0) {
                 const unsigned long long t0 = global_ns();
@@ -984,15 +1033,24 @@ bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
     // per slab); two landing tiles when that still leaves room for two held slabs.
     p.tiles_per_group = (p.n_tiles_max + 1) / 2;
     const int slab_cols = p.tiles_per_group * 16;
-    p.land = 2;
-    p.held = (kTmemCols / 2 - p.land * kRP) / slab_cols;
-    if (p.held < 2) {
-        p.land = 1;
+    p.lse_mode = q.lse_mode ? 1 : 0;
+    p.lse_in = q.lse_in;
+    if (p.lse_mode) {
+        // no held logits: all of TMEM holds landing tiles
+        p.land = kMaxLand;
+        p.held = 0;
+        p.lag = 0;
+    } else {
+        p.land = 2;
         p.held = (kTmemCols / 2 - p.land * kRP) / slab_cols;
+        if (p.held < 2) {
+            p.land = 1;
+            p.held = (kTmemCols / 2 - p.land * kRP) / slab_cols;
+        }
+        if (p.held < 1) return false;
+        p.held = std::min(p.held, kMaxHeld);
+        p.lag = p.held - 1;
     }
-    if (p.held < 1) return false;
-    p.held = std::min(p.held, kMaxHeld);
-    p.lag = p.held - 1;
     p.held_base = 2 * p.land * kRP;               // after both groups' landing tiles
     if (p.held_base + 2 * p.held * slab_cols > kTmemCols) return false;
     p.scale = 1.0f / sqrtf((float)q.d);

@@ -42,7 +42,9 @@ const char* last_error_text();
 struct ScoreProblem {
     const void* Q;          // [B, N, L, H, d]
     const void* K;          // [L, H_kv, T, d]
-    const void* Kla;        // [B, L, H_kv, N, d]
+    const void* Kla;        // [B, L, H_kv, N, d]; unused when lse_in is given
+    const float* lse_in;    // [L, H, N] softmax normalisers given by the caller (lse_mode)
+    bool lse_mode;          // sp_score_lse: lse_in replaces the statistics pass
     float* importance;      // [T]
     const int64_t* cu_M_host;   // [B+1] host copy
     int B, L, H, H_kv, d, N;

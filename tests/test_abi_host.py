@@ -109,3 +109,17 @@ def test_calls_without_gpu_fail_cleanly(sp):
         pytest.skip("a GPU is present")
     need = sp.sp_select_workspace_size(512, 32)
     assert sp.sp_select(16, 512, 32, 3, 0, 0.3, None, 16, 16, 16, need, 0) == sp.SP_ECUDA
+
+
+def test_score_lse_validation(sp):
+    """sp_score_lse: same shape rules as sp_score; the lse pointer replaces K_la (4-byte aligned)."""
+    need = sp.sp_score_lse_workspace_size(2, 4, 2, 64, 512, 4, sp.SP_F32)
+    assert need > 0
+    assert sp.sp_score_lse_workspace_size(2, 5, 2, 64, 512, 4, sp.SP_F32) == 0          # H % H_kv != 0
+    f = sp.sp_score_lse
+    assert f(16, 16, 16, 2, 4, 2, 12, 512, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EUNSUPPORTED   # d
+    assert f(16, 16, 16, 2, 4, 2, 64, -1, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL          # M
+    assert f(16, 16, 16, 2, 4, 2, 64, 512, 4, sp.SP_F32, 16, 16, need - 1, 0) == sp.SP_ENOMEM
+    assert f(16, 16, None, 2, 4, 2, 64, 512, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL       # null lse
+    assert f(16, 16, 18, 2, 4, 2, 64, 512, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL         # misaligned lse
+    assert "aligned" in sp.sp_last_error()

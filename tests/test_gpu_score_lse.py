@@ -1,0 +1,86 @@
+"""Parity of sp_score_lse (single pass, each row's lse given) with the fp64
+oracle, element by element.
+
+The lse given to the kernel is the oracle's row_lse rounded to fp32, and the
+oracle's importance_given_lse reads the same fp32 values.  The cases cover the
+general path (fp32), the tensor-core path (bf16 8B shape) with 1 to 8 slab
+classes, ragged tails, and N = 0.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_helpers import check_importance, config_inputs, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import torch
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    from speculative_prefill_token_sp_gb300 import build
+    build.build()
+    import speculative_prefill_token_sp_gb300 as m
+    m.lib()
+    return m
+
+
+def run_lse(sp, x, lse32):
+    import torch
+    Q, K = to_device(x.Q_la), to_device(x.K_prompt)
+    imp = sp.score_lse(Q, K, torch.from_numpy(lse32).cuda(), check=True)
+    torch.cuda.synchronize()
+    return imp.cpu().numpy()
+
+
+def check_case(sp, x, what):
+    lse32 = oracle.row_lse(x.Q_la, x.K_prompt, x.K_la).astype(np.float32)
+    got = run_lse(sp, x, lse32)
+    ref = oracle.importance_given_lse(x.Q_la, x.K_prompt, lse32.astype(np.float64))
+    check_importance(got, ref, x.wl.dtype, what)
+
+
+@pytest.mark.parametrize("index", [0, 1])
+def test_config_parity(sp, index):
+    x = config_inputs(index)
+    check_case(sp, x, x.wl.name)
+
+
+SHAPES = [
+    # (L, H, H_kv, d, M, N, dtype)
+    (1, 1, 1, 64, 1, 1, "bf16"),
+    (2, 4, 2, 128, 129, 3, "bf16"),
+    (3, 8, 8, 64, 300, 1, "bf16"),
+    (1, 32, 4, 128, 4097, 8, "bf16"),
+    (2, 6, 3, 72, 513, 5, "bf16"),         # general path (d = 72)
+    (1, 16, 2, 256, 257, 4, "f32"),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "L{}H{}Hkv{}d{}M{}N{}{}".format(*s))
+def test_random_shapes(sp, shape):
+    L, H, H_kv, d, M, N, dt = shape
+    wl = W.Workload("t", L=L, H=H, H_kv=H_kv, d=d, M=M, N=N, dtype=dt, chunk=16, pool_k=3, mode="topk",
+                    keep_rate=0.3, needle_frac=0.05, run_min=2, run_max=8)
+    check_case(sp, W.make_inputs(wl, seed=2000 + M), str(shape))
+
+
+@pytest.mark.parametrize("M", [40960, 131072])
+def test_long_prompts_few_layers(sp, M):
+    wl = W.Workload("t", L=1, H=32, H_kv=8, d=128, M=M, N=8, dtype="bf16", chunk=64, pool_k=3, mode="topk",
+                    keep_rate=0.1, needle_frac=0.01, run_min=16, run_max=128)
+    check_case(sp, W.make_inputs(wl, seed=M + 1), f"M={M}")
+
+
+def test_zero_lookahead_gives_ones(sp):
+    import torch
+    K = torch.randn(2, 2, 50, 64, device="cuda").to(torch.bfloat16)
+    Q = torch.empty(0, 2, 4, 64, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(2, 4, 0, device="cuda")
+    imp = sp.score_lse(Q, K, lse)
+    torch.cuda.synchronize()
+    assert torch.all(imp == 1.0)
