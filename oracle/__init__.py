@@ -39,3 +39,4 @@ from .select import (  # noqa: F401
     chunk_sums, chunk_means, avg_pool, keep_count, topk_chunks, normalize_boost,
     mass_chunks, kept_positions, select, select_varlen,
 )
+from .gather import gather_kept  # noqa: F401,E402
