@@ -231,6 +231,29 @@ sp_status sp_select_noalloc(const float* importance, int64_t M, int chunk, int p
                             void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Sparse-prefill input                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* The target's sparse-prefill batch: for B packed prompts, each prompt's kept
+ * token IDs and original position IDs, packed prompt after prompt (paper
+ * review, "core algorithm: position ID recovery": the kept tokens keep their
+ * positions and decoding continues at M_b, M_b + 1, ...).
+ *
+ *   token_ids     [T] int32, packed by cu_M_host (needed only if out_tokens is given)
+ *   kept_pos      [T] int32, prompt b's ascending kept positions (relative to its
+ *                 start) at kept_pos[cu_M[b] ...], as sp_select_varlen writes them
+ *   n_kept        device int64[B], as sp_select_varlen writes it
+ *   out_tokens    [T] int32 capacity or NULL: out_tokens[cu_kept[b] + i] = token_ids[cu_M[b] + kept_pos[cu_M[b] + i]]
+ *   out_positions [T] int32 capacity or NULL: out_positions[cu_kept[b] + i] = kept_pos[cu_M[b] + i]
+ *   cu_kept       device int64[B + 1]: prefix sums of n_kept
+ *
+ * Requirements: 1 <= B <= 256, cu_M_host as for sp_select_varlen; at least one
+ * of out_tokens / out_positions.  No workspace. */
+sp_status sp_gather_kept(const int32_t* token_ids, int B, const int64_t* cu_M_host, const int32_t* kept_pos,
+                         const int64_t* n_kept, int32_t* out_tokens, int32_t* out_positions, int64_t* cu_kept,
+                         void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                   */
 /* ------------------------------------------------------------------------ */
 

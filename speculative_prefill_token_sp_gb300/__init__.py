@@ -20,9 +20,9 @@ __all__ = [
     "sp_score_workspace_size", "sp_score", "sp_score_lse_workspace_size", "sp_score_lse",
     "sp_score_varlen_workspace_size", "sp_score_varlen",
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
-    "sp_select_noalloc", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
+    "sp_select_noalloc", "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
     "sp_kernel_launches",
-    "score", "score_lse", "score_varlen", "select", "select_varlen", "V3_BOOST",
+    "score", "score_lse", "score_varlen", "select", "select_varlen", "gather_kept", "V3_BOOST",
 ]
 
 SP_OK, SP_EINVAL, SP_ENOMEM, SP_ECUDA, SP_EDEVICE, SP_ETIMEOUT, SP_EUNSUPPORTED = range(7)
@@ -66,6 +66,7 @@ _SIGS = {
     "sp_select_varlen_workspace_size": (_sz, [_i32, _vp, _i32]),
     "sp_select_varlen": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sp_select_noalloc": (_i32, [_vp, _i64, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp]),
+    "sp_gather_kept": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "sp_workspace_status": (_i32, [_vp, _vp]),
     "sp_last_error": (_c.c_char_p, []),
     "sp_status_string": (_c.c_char_p, [_i32]),
@@ -190,6 +191,13 @@ def sp_select_noalloc(importance, M, chunk, pool_k, mode, rate, boost, kept_pos,
     """sp_select without a workspace (scratch in a fixed device array of the library)."""
     return lib().sp_select_noalloc(_ptr(importance), M, chunk, pool_k, mode, rate, _boost(boost), _ptr(kept_pos),
                                    _ptr(n_kept), _stream(stream))
+
+
+def sp_gather_kept(token_ids, B, cu_M_host, kept_pos, n_kept, out_tokens, out_positions, cu_kept,
+                   stream=None) -> int:
+    cu = _i64_array(cu_M_host)
+    return lib().sp_gather_kept(_ptr(token_ids), B, ctypes.addressof(cu), _ptr(kept_pos), _ptr(n_kept),
+                                _ptr(out_tokens), _ptr(out_positions), _ptr(cu_kept), _stream(stream))
 
 
 def sp_workspace_status(ws, stream=None) -> int:
@@ -338,3 +346,17 @@ def select_varlen(importance, cu_M, chunk, pool_k, mode, rate, boost=None, *, ke
         n = n_kept.tolist()
         return [kept_pos[cu[b]: cu[b] + n[b]] for b in range(B)]
     return kept_pos, n_kept
+
+
+def gather_kept(token_ids, cu_M, kept_pos, n_kept, *, stream=None):
+    """Sparse-prefill batch of packed prompts: (tokens int32, positions int32, cu_kept int64 [B+1]),
+    each prompt's kept tokens packed after the previous prompt's (device tensors, capacity T)."""
+    import torch
+    cu = [int(x) for x in cu_M]
+    B, T = len(cu) - 1, cu[-1]
+    dev = kept_pos.device
+    tokens = torch.empty(max(T, 1), dtype=torch.int32, device=dev)
+    positions = torch.empty(max(T, 1), dtype=torch.int32, device=dev)
+    cu_kept = torch.empty(B + 1, dtype=torch.int64, device=dev)
+    _check(sp_gather_kept(token_ids, B, cu, kept_pos, n_kept, tokens, positions, cu_kept, stream))
+    return tokens, positions, cu_kept

@@ -33,6 +33,11 @@ std::atomic<uint64_t> g_launches{0};
 }
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Implemented in gather.cu.
+sp_status gather_launch(const int32_t* token_ids, int B, const int64_t* cu_M_host, const int32_t* kept_pos,
+                        const int64_t* n_kept, int32_t* out_tokens, int32_t* out_positions, int64_t* cu_kept,
+                        cudaStream_t st);
+
 // Implemented in score_tc.cu: the tensor-core path for the bf16 shapes it covers.
 bool score_tc_supported(const ScoreProblem& p);
 size_t score_tc_ws_bytes(const ScoreProblem& p);
@@ -320,6 +325,22 @@ sp_status sp_score_varlen(const void* Q_la, const void* K_prompt, const void* K_
     ScoreProblem p = make_score_problem(Q_la, K_prompt, K_la, B, cu_M_host, L, H, H_kv, d, N, dtype,
                                         importance);
     return run_score("sp_score_varlen", p, ws, ws_bytes, stream);
+}
+
+sp_status sp_gather_kept(const int32_t* token_ids, int B, const int64_t* cu_M_host, const int32_t* kept_pos,
+                         const int64_t* n_kept, int32_t* out_tokens, int32_t* out_positions, int64_t* cu_kept,
+                         void* stream) {
+    sp_status s = check_cu("sp_gather_kept", B, cu_M_host);
+    if (s != SP_OK) return s;
+    if (!kept_pos || !n_kept || !cu_kept || (out_tokens && !token_ids) || (!out_tokens && !out_positions)) {
+        set_error("sp_gather_kept: null pointer (kept_pos, n_kept, cu_kept, and token_ids when tokens are gathered; "
+                  "at least one output)");
+        return SP_EINVAL;
+    }
+    s = gather_launch(token_ids, B, cu_M_host, kept_pos, n_kept, out_tokens, out_positions, cu_kept,
+                      static_cast<cudaStream_t>(stream));
+    if (s == SP_OK) clear_error();
+    return s;
 }
 
 size_t sp_select_workspace_size(int64_t M, int chunk) {

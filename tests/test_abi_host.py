@@ -123,3 +123,12 @@ def test_score_lse_validation(sp):
     assert f(16, 16, None, 2, 4, 2, 64, 512, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL       # null lse
     assert f(16, 16, 18, 2, 4, 2, 64, 512, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL         # misaligned lse
     assert "aligned" in sp.sp_last_error()
+
+
+def test_gather_validation(sp):
+    f = sp.sp_gather_kept
+    assert f(16, 0, [0], 16, 16, 16, 16, 16, 0) == sp.SP_EINVAL                 # B < 1
+    assert f(16, 2, [0, 5, 3], 16, 16, 16, 16, 16, 0) == sp.SP_EINVAL           # decreasing offsets
+    assert f(16, 1, [0, 5], None, 16, 16, 16, 16, 0) == sp.SP_EINVAL            # no kept_pos
+    assert f(None, 1, [0, 5], 16, 16, 16, None, 16, 0) == sp.SP_EINVAL          # tokens wanted, no token_ids
+    assert f(16, 1, [0, 5], 16, 16, None, None, 16, 0) == sp.SP_EINVAL          # no output at all
