@@ -37,6 +37,6 @@ pinned by the tests only as far as the mathematics allows):
 from .score import importance, attention_rows, lookahead_rows, row_lse, importance_given_lse  # noqa: F401
 from .select import (  # noqa: F401
     chunk_sums, chunk_means, avg_pool, keep_count, topk_chunks, normalize_boost,
-    mass_chunks, kept_positions, select, select_varlen,
+    mass_chunks, kept_positions, select, select_varlen, keep_rules, select_mask, select_rules,
 )
 from .gather import gather_kept  # noqa: F401,E402

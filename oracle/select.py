@@ -164,8 +164,8 @@ def kept_positions(mask, chunk: int, M: int) -> np.ndarray:
     return np.asarray(out, dtype=np.int32)
 
 
-def select(importance, chunk: int, pool_k: int, mode: str, rate: float, boost=None):
-    """Whole selection step.  Returns (kept_pos int32[n_kept], n_kept).
+def select_mask(importance, chunk: int, pool_k: int, mode: str, rate: float, boost=None):
+    """The chunk mask of the selection step (see select) and the prompt length.
 
     mode "topk": rate = keep_rate; chunk means -> avg pool (pool_k) -> top-kc.
     mode "mass": rate = tau; chunk means rank the chunks, chunk sums are the
@@ -186,7 +186,26 @@ def select(importance, chunk: int, pool_k: int, mode: str, rate: float, boost=No
         mask = mass_chunks(sums, means, rate)
     else:
         raise ValueError(mode)
+    return mask, M
+
+
+def select(importance, chunk: int, pool_k: int, mode: str, rate: float, boost=None):
+    """Whole selection step.  Returns (kept_pos int32[n_kept], n_kept).
+
+    mode "topk": rate = keep_rate; chunk means -> avg pool (pool_k) -> top-kc.
+    mode "mass": rate = tau; chunk means rank the chunks, chunk sums are the
+    mass; pool_k must be 1.
+    """
+    mask, M = select_mask(importance, chunk, pool_k, mode, rate, boost)
     pos = kept_positions(mask, chunk, M)
+    return pos, int(pos.shape[0])
+
+
+def select_rules(importance, chunk: int, pool_k: int, mode: str, rate: float, boost=None, *,
+                 min_tok: int = 0, always_keep: bool = False, max_keep: int = 0):
+    """select() followed by keep_rules(): (kept_pos int32[n_kept], n_kept)."""
+    mask, M = select_mask(importance, chunk, pool_k, mode, rate, boost)
+    pos = keep_rules(kept_positions(mask, chunk, M), mask, M, chunk, min_tok, always_keep, max_keep)
     return pos, int(pos.shape[0])
 
 
@@ -195,3 +214,55 @@ def select_varlen(importance_packed, cu_M, chunk, pool_k, mode, rate, boost=None
     cu = np.asarray(cu_M, dtype=np.int64)
     return [select(importance_packed[cu[b]:cu[b + 1]], chunk, pool_k, mode, rate, boost)
             for b in range(cu.shape[0] - 1)]
+
+
+def keep_rules(kept, mask, M: int, chunk: int, min_tok: int = 0, always_keep: bool = False,
+               max_keep: int = 0) -> np.ndarray:
+    """The guide's v2 keep rules on top of a chunk selection (llama.cpp guide,
+    "Full Source Code": select_chunks' always-kept tokens and minimum-token
+    back-fill, and the sparse-prefill cap SP_MAX_KEEP of its main program).
+
+    kept: the selection's ascending positions; mask: its chunk mask.
+      * min_tok > 0: eff_min = min(min_tok, max(4, M // 10)); a prompt of at
+        most eff_min tokens keeps every token;
+      * always_keep: tokens 0, 1, 2, 3 and, if M > 4, M - 2 and M - 1 are kept;
+      * while fewer than eff_min tokens are kept, tokens of the chunks the
+        selection left out join, chunk by chunk in index order and token by
+        token, skipping tokens already kept;
+      * the result is ascending;
+      * max_keep > 0 and n > max_keep kept: every step-th kept token, step =
+        n // max_keep, at most max_keep of them, the last of which is replaced
+        by the last kept token.
+    """
+    mask = np.asarray(mask, dtype=bool)
+    out = [int(p) for p in kept]
+    eff_min = min(min_tok, max(4, M // 10)) if min_tok > 0 else 0
+    if M <= eff_min:
+        out = list(range(M))
+    else:
+        have = set(out)
+        if always_keep:
+            for a in [0, 1, 2, 3] + ([M - 2, M - 1] if M > 4 else []):
+                if a < M and a not in have:
+                    out.append(a)
+                    have.add(a)
+        if len(out) < eff_min:
+            for c in range(len(mask)):
+                if len(out) >= eff_min:
+                    break
+                if mask[c]:
+                    continue
+                for i in range(c * chunk, min((c + 1) * chunk, M)):
+                    if len(out) >= eff_min:
+                        break
+                    if i not in have:
+                        out.append(i)
+                        have.add(i)
+        out.sort()
+    if max_keep > 0 and len(out) > max_keep:
+        step = len(out) // max_keep
+        capped = [out[i] for i in range(0, len(out), step)][:max_keep]
+        if capped[-1] != out[-1]:
+            capped[-1] = out[-1]
+        out = capped
+    return np.asarray(out, dtype=np.int32)
