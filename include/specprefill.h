@@ -78,6 +78,21 @@ typedef struct {
     int32_t normalize;
 } sp_boost;
 
+/* The guide's v2 keep rules applied after the chunk selection (llama.cpp
+ * guide, "Full Source Code": select_chunks and its main program's sparse-
+ * prefill cap).  min_tok > 0 sets eff_min = min(min_tok, max(4, M / 10)): a
+ * prompt of at most eff_min tokens keeps every token, otherwise tokens of the
+ * chunks the selection left out are added, chunk by chunk and token by token
+ * in order, until eff_min are kept.  always_keep != 0 adds tokens 0, 1, 2, 3
+ * and, if M > 4, M-2 and M-1.  max_keep > 0 caps the result: with n > max_keep
+ * kept, every (n / max_keep)-th token is kept, at most max_keep, the last one
+ * replaced by the last kept token.  The guide runs with {128, 1, 2000}. */
+typedef struct {
+    int32_t min_tok;        /* 0 = off; at most 4096 */
+    int32_t always_keep;
+    int64_t max_keep;       /* 0 = no cap */
+} sp_keep_rules;
+
 /* ------------------------------------------------------------------------ */
 /* Scoring                                                                  */
 /* ------------------------------------------------------------------------ */
@@ -194,6 +209,17 @@ size_t sp_select_workspace_size(int64_t M, int chunk);
 sp_status sp_select(const float* importance, int64_t M, int chunk, int pool_k, sp_mode mode,
                     double rate, const sp_boost* boost, int32_t* kept_pos, int64_t* n_kept,
                     void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for sp_select_rules. */
+size_t sp_select_rules_workspace_size(int64_t M, int chunk);
+
+/* sp_select followed by the keep rules (sp_keep_rules) on the same prompt.
+ * kept_pos receives the final ascending positions (capacity M) and n_kept
+ * their count.  rules == NULL behaves as sp_select.  Errors: SP_EINVAL for a
+ * negative min_tok or max_keep, SP_EUNSUPPORTED for min_tok > 4096. */
+sp_status sp_select_rules(const float* importance, int64_t M, int chunk, int pool_k, sp_mode mode,
+                          double rate, const sp_boost* boost, const sp_keep_rules* rules,
+                          int32_t* kept_pos, int64_t* n_kept, void* ws, size_t ws_bytes, void* stream);
 
 /* Workspace bytes for sp_select_varlen. */
 size_t sp_select_varlen_workspace_size(int B, const int64_t* cu_M_host, int chunk);

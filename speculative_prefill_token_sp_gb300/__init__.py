@@ -20,9 +20,10 @@ __all__ = [
     "sp_score_workspace_size", "sp_score", "sp_score_lse_workspace_size", "sp_score_lse",
     "sp_score_varlen_workspace_size", "sp_score_varlen",
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
-    "sp_select_noalloc", "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
+    "sp_select_noalloc", "sp_select_rules_workspace_size", "sp_select_rules", "SpKeepRules", "GUIDE_RULES",
+    "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
     "sp_kernel_launches",
-    "score", "score_lse", "score_varlen", "select", "select_varlen", "gather_kept", "V3_BOOST",
+    "score", "score_lse", "score_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
 ]
 
 SP_OK, SP_EINVAL, SP_ENOMEM, SP_ECUDA, SP_EDEVICE, SP_ETIMEOUT, SP_EUNSUPPORTED = range(7)
@@ -42,6 +43,15 @@ class SpBoost(ctypes.Structure):
 
 # The llama.cpp guide's v3 defaults: first 64 tokens x1.5, last 128 x1.3, normalised.
 V3_BOOST = (64, 1.5, 128, 1.3, 1)
+
+
+class SpKeepRules(ctypes.Structure):
+    """sp_keep_rules: the guide's v2 keep rules after the chunk selection."""
+    _fields_ = [("min_tok", ctypes.c_int32), ("always_keep", ctypes.c_int32), ("max_keep", ctypes.c_int64)]
+
+
+# The rules the llama.cpp guide runs with: min_tok 128, always-kept tokens, SP_MAX_KEEP 2000.
+GUIDE_RULES = (128, 1, 2000)
 
 
 class SpError(RuntimeError):
@@ -66,6 +76,8 @@ _SIGS = {
     "sp_select_varlen_workspace_size": (_sz, [_i32, _vp, _i32]),
     "sp_select_varlen": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sp_select_noalloc": (_i32, [_vp, _i64, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp]),
+    "sp_select_rules_workspace_size": (_sz, [_i64, _i32]),
+    "sp_select_rules": (_i32, [_vp, _i64, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sp_gather_kept": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "sp_workspace_status": (_i32, [_vp, _vp]),
     "sp_last_error": (_c.c_char_p, []),
@@ -172,6 +184,24 @@ def sp_select(importance, M, chunk, pool_k, mode, rate, boost, kept_pos, n_kept,
               stream=None) -> int:
     return lib().sp_select(_ptr(importance), M, chunk, pool_k, mode, rate, _boost(boost), _ptr(kept_pos),
                            _ptr(n_kept), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def _rules(rules):
+    if rules is None:
+        return None
+    if isinstance(rules, SpKeepRules):
+        return ctypes.pointer(rules)
+    return ctypes.pointer(SpKeepRules(*rules))
+
+
+def sp_select_rules_workspace_size(M, chunk) -> int:
+    return lib().sp_select_rules_workspace_size(M, chunk)
+
+
+def sp_select_rules(importance, M, chunk, pool_k, mode, rate, boost, rules, kept_pos, n_kept, ws, ws_bytes,
+                    stream=None) -> int:
+    return lib().sp_select_rules(_ptr(importance), M, chunk, pool_k, mode, rate, _boost(boost), _rules(rules),
+                                 _ptr(kept_pos), _ptr(n_kept), _ptr(ws), ws_bytes, _stream(stream))
 
 
 def sp_select_varlen_workspace_size(B, cu_M_host, chunk) -> int:
@@ -326,6 +356,19 @@ def select(importance, chunk, pool_k, mode, rate, boost=None, *, kept_pos=None, 
     if trim:
         return kept_pos[: int(n_kept.item())]
     return kept_pos, n_kept
+
+
+def select_rules(importance, chunk, pool_k, mode, rate, boost=None, rules=GUIDE_RULES, *, ws=None, stream=None):
+    """Kept position IDs of one prompt after the selection and the keep rules (synchronises)."""
+    import torch
+    M = importance.shape[0]
+    dev = importance.device
+    kept_pos = torch.empty(max(M, 1), dtype=torch.int32, device=dev)
+    n_kept = torch.empty(1, dtype=torch.int64, device=dev)
+    ws = _workspace(sp_select_rules_workspace_size(M, chunk), dev, ws)
+    _check(sp_select_rules(importance, M, chunk, pool_k, _mode(mode), float(rate), boost, rules, kept_pos, n_kept,
+                           ws, ws.numel(), stream))
+    return kept_pos[: int(n_kept.item())]
 
 
 def select_varlen(importance, cu_M, chunk, pool_k, mode, rate, boost=None, *, kept_pos=None, n_kept=None,

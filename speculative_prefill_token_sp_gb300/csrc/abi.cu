@@ -200,6 +200,8 @@ SelectProblem make_select_problem(const float* imp, int B, const int64_t* cu, in
     if (boost) p.boost = *boost;
     else p.boost = sp_boost{0, 1.0, 0, 1.0, 0};
     p.kept_pos = kept; p.n_kept = n_kept;
+    p.has_rules = false;
+    p.rules = sp_keep_rules{0, 0, 0};
     p.max_M = 0; p.total_chunks = 0; p.max_nc = 0;
     for (int b = 0; b < B; ++b) {
         const int64_t Mb = cu[b + 1] - cu[b];
@@ -363,6 +365,40 @@ sp_status sp_select(const float* importance, int64_t M, int chunk, int pool_k, s
     SelectProblem p = make_select_problem(importance, 1, cu, chunk, pool_k, mode, rate, boost, kept_pos,
                                           n_kept);
     return run_select("sp_select", p, ws, ws_bytes, stream);
+}
+
+size_t sp_select_rules_workspace_size(int64_t M, int chunk) {
+    if (M < 0 || chunk < 1) return 0;
+    int64_t cu[2] = {0, M};
+    SelectProblem p = make_select_problem(nullptr, 1, cu, chunk, 1, SP_SELECT_TOPK, 1.0, nullptr, nullptr, nullptr);
+    p.has_rules = true;
+    return select_ws_bytes(p);
+}
+
+sp_status sp_select_rules(const float* importance, int64_t M, int chunk, int pool_k, sp_mode mode, double rate,
+                          const sp_boost* boost, const sp_keep_rules* rules, int32_t* kept_pos, int64_t* n_kept,
+                          void* ws, size_t ws_bytes, void* stream) {
+    if (M < 0 || M > (int64_t)INT32_MAX) {
+        set_error("sp_select_rules: M must be in [0, 2^31-1] (got %lld)", (long long)M);
+        return M < 0 ? SP_EINVAL : SP_EUNSUPPORTED;
+    }
+    sp_status s = check_select_params("sp_select_rules", chunk, pool_k, mode, rate, boost);
+    if (s != SP_OK) return s;
+    if (rules && (rules->min_tok < 0 || rules->max_keep < 0)) {
+        set_error("sp_select_rules: min_tok and max_keep must be >= 0");
+        return SP_EINVAL;
+    }
+    if (rules && rules->min_tok > 4096) {
+        set_error("sp_select_rules: min_tok is at most 4096 (got %d)", rules->min_tok);
+        return SP_EUNSUPPORTED;
+    }
+    int64_t cu[2] = {0, M};
+    SelectProblem p = make_select_problem(importance, 1, cu, chunk, pool_k, mode, rate, boost, kept_pos, n_kept);
+    if (rules) {
+        p.has_rules = true;
+        p.rules = *rules;
+    }
+    return run_select("sp_select_rules", p, ws, ws_bytes, stream);
 }
 
 size_t sp_select_varlen_workspace_size(int B, const int64_t* cu_M_host, int chunk) {

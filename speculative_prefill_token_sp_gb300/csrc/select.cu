@@ -30,6 +30,8 @@ namespace {
 constexpr int kMaxBatch = 256;
 constexpr int kSelThreads = 1024;
 constexpr int kMassMaxChunks = 16384;
+constexpr int kMaxMinTok = 4096;        // keep-rule minimum, at most
+constexpr int kMaxExtras = kMaxMinTok + 6;
 
 struct SelGeo {
     int B, chunk, pool_k;
@@ -40,6 +42,8 @@ struct SelGeo {
     double first_mult, last_mult;
     int64_t cu[kMaxBatch + 1];      // token offsets
     int64_t cn[kMaxBatch + 1];      // chunk offsets
+    int min_tok, always_keep;       // keep rules (sp_select_rules)
+    int64_t max_keep;
 };
 
 // IEEE order of doubles as unsigned integers (+0 and -0 map to the same key).
@@ -333,8 +337,102 @@ __global__ void compact_kernel(const SelGeo g, const int* __restrict__ flags,
     }
 }
 
+// (5) the guide's v2 keep rules on one prompt's selection (llama.cpp guide,
+// "Full Source Code": select_chunks' always-kept tokens and minimum-token
+// back-fill, the main program's SP_MAX_KEEP cap), one block per prompt:
+//   eff_min = min(min_tok, max(4, M / 10)); M <= eff_min keeps every token;
+//   always_keep adds tokens 0..3 and, if M > 4, M-2 and M-1;
+//   while fewer than eff_min are kept, tokens of unselected chunks join in
+//   chunk, then token order; the result is ascending;
+//   more than max_keep (> 0): every (n / max_keep)-th token, at most max_keep,
+//   the last replaced by the last kept token.
+__global__ void __launch_bounds__(1024) rules_kernel(const SelGeo g, const int* __restrict__ flags,
+                                                     int32_t* __restrict__ kept_pos, int64_t* __restrict__ n_kept,
+                                                     int32_t* __restrict__ scratch) {
+    __shared__ int32_t extra[kMaxExtras];
+    __shared__ int n_extra;
+    __shared__ int64_t total_sh;
+    const int b = blockIdx.x;
+    const int64_t m0 = g.cu[b], M = g.cu[b + 1] - m0;
+    const int64_t c0 = g.cn[b], nc = g.cn[b + 1] - c0;
+    int32_t* kept = kept_pos + m0;
+    int32_t* S = scratch + m0;                   // merged list
+    const int64_t n = n_kept[b];
+    const int64_t eff_min = g.min_tok > 0 ? min((int64_t)g.min_tok, max((int64_t)4, M / 10)) : 0;
+    if (M == 0) return;
+    if (M <= eff_min) {
+        for (int64_t i = threadIdx.x; i < M; i += blockDim.x) S[i] = (int32_t)i;
+        if (threadIdx.x == 0) total_sh = M;
+    } else {
+        if (threadIdx.x == 0) {
+            // tokens to add, ascending: always-kept ones outside kept chunks, then the
+            // back-fill (distinct from kept tokens by construction, and checked
+            // against the always-kept ones)
+            int32_t always[6];
+            int na = 0;
+            if (g.always_keep) {
+                const int64_t cand[6] = {0, 1, 2, 3, M - 2, M - 1};
+                const int nc6 = M > 4 ? 6 : 4;
+                for (int k = 0; k < nc6; ++k) {
+                    const int64_t a = cand[k];
+                    if (a < M && !flags[c0 + a / g.chunk]) always[na++] = (int32_t)a;
+                }
+            }
+            int64_t have = n + na;
+            int m = 0;
+            for (int64_t c = 0; c < nc && have < eff_min; ++c) {
+                if (flags[c0 + c]) continue;
+                const int64_t e = min((c + 1) * (int64_t)g.chunk, M);
+                for (int64_t i = c * g.chunk; i < e && have < eff_min; ++i) {
+                    bool dup = false;
+                    for (int k = 0; k < na; ++k) dup |= always[k] == (int32_t)i;
+                    if (!dup) { extra[m++] = (int32_t)i; ++have; }
+                }
+            }
+            // insert the always-kept tokens into the ascending back-fill list
+            for (int k = 0; k < na; ++k) {
+                int pos = m++;
+                while (pos > 0 && extra[pos - 1] > always[k]) { extra[pos] = extra[pos - 1]; --pos; }
+                extra[pos] = always[k];
+            }
+            n_extra = m;
+            total_sh = n + m;
+        }
+        __syncthreads();
+        const int m = n_extra;
+        // merge: a kept token moves right by the extras below it, an extra by the kept tokens below it
+        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+            const int32_t v = kept[i];
+            int lo = 0, hi = m;
+            while (lo < hi) { const int mid = (lo + hi) >> 1; if (extra[mid] < v) lo = mid + 1; else hi = mid; }
+            S[i + lo] = v;
+        }
+        for (int k = threadIdx.x; k < m; k += blockDim.x) {
+            const int32_t v = extra[k];
+            int64_t lo = 0, hi = n;
+            while (lo < hi) { const int64_t mid = (lo + hi) >> 1; if (kept[mid] < v) lo = mid + 1; else hi = mid; }
+            S[k + lo] = v;
+        }
+    }
+    __syncthreads();
+    const int64_t total = total_sh;
+    if (g.max_keep > 0 && total > g.max_keep) {
+        const int64_t step = total / g.max_keep;
+        const int64_t cnt = min(g.max_keep, (total + step - 1) / step);
+        for (int64_t k = threadIdx.x; k < cnt; k += blockDim.x) kept[k] = S[k * step];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (kept[cnt - 1] != S[total - 1]) kept[cnt - 1] = S[total - 1];
+            n_kept[b] = cnt;
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < total; k += blockDim.x) kept[k] = S[k];
+        if (threadIdx.x == 0) n_kept[b] = total;
+    }
+}
+
 struct SelLayout {
-    size_t mm, sums, means, pooled, flags, offs, total;
+    size_t mm, sums, means, pooled, flags, offs, scratch, total;
 };
 
 SelLayout sel_layout(const SelectProblem& p) {
@@ -347,6 +445,7 @@ SelLayout sel_layout(const SelectProblem& p) {
     lo.pooled = c.take(sizeof(double) * nc);
     lo.flags = c.take(sizeof(int) * nc);
     lo.offs = c.take(sizeof(int64_t) * nc);
+    lo.scratch = p.has_rules ? c.take(sizeof(int32_t) * (size_t)std::max<int64_t>(p.T, 1)) : c.off;
     lo.total = c.off;
     return lo;
 }
@@ -370,6 +469,9 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     g.has_boost = p.has_boost ? 1 : 0;
     g.first_n = p.boost.first_n; g.last_n = p.boost.last_n; g.normalize = p.boost.normalize;
     g.first_mult = p.boost.first_mult; g.last_mult = p.boost.last_mult;
+    g.min_tok = p.has_rules ? p.rules.min_tok : 0;
+    g.always_keep = p.has_rules ? p.rules.always_keep : 0;
+    g.max_keep = p.has_rules ? p.rules.max_keep : 0;
     g.cu[0] = 0; g.cn[0] = 0;
     for (int b = 0; b < p.B; ++b) {
         g.cu[b + 1] = p.cu_M_host[b + 1];
@@ -414,6 +516,11 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     if (p.T > 0) {
         const int blocks = (int)std::min<int64_t>((p.T + 255) / 256, 4096);
         compact_kernel<<<blocks, 256, 0, st>>>(g, flags, offs, p.kept_pos);
+        SP_LAUNCH_CHECK();
+    }
+    if (p.has_rules && p.T > 0) {
+        rules_kernel<<<p.B, 1024, 0, st>>>(g, flags, p.kept_pos, p.n_kept,
+                                           reinterpret_cast<int32_t*>(w + lo.scratch));
         SP_LAUNCH_CHECK();
     }
     return SP_OK;

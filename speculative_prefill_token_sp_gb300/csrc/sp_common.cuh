@@ -68,6 +68,8 @@ struct SelectProblem {
     sp_boost boost;
     int32_t* kept_pos;          // [T]
     int64_t* n_kept;            // [B]
+    bool has_rules;             // the guide's v2 keep rules (sp_select_rules)
+    sp_keep_rules rules;
 };
 size_t select_ws_bytes(const SelectProblem& p);
 sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st);

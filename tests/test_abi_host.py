@@ -132,3 +132,13 @@ def test_gather_validation(sp):
     assert f(16, 1, [0, 5], None, 16, 16, 16, 16, 0) == sp.SP_EINVAL            # no kept_pos
     assert f(None, 1, [0, 5], 16, 16, 16, None, 16, 0) == sp.SP_EINVAL          # tokens wanted, no token_ids
     assert f(16, 1, [0, 5], 16, 16, None, None, 16, 0) == sp.SP_EINVAL          # no output at all
+
+
+def test_select_rules_validation(sp):
+    need = sp.sp_select_rules_workspace_size(512, 32)
+    assert need > sp.sp_select_workspace_size(512, 32)          # scratch for the merged list
+    f = sp.sp_select_rules
+    assert f(16, 512, 32, 3, 0, 0.3, None, (-1, 1, 0), 16, 16, 16, need, 0) == sp.SP_EINVAL
+    assert f(16, 512, 32, 3, 0, 0.3, None, (128, 1, -5), 16, 16, 16, need, 0) == sp.SP_EINVAL
+    assert f(16, 512, 32, 3, 0, 0.3, None, (5000, 1, 0), 16, 16, 16, need, 0) == sp.SP_EUNSUPPORTED
+    assert f(16, 512, 32, 3, 0, 0.3, None, sp.GUIDE_RULES, 16, 16, 16, need - 1, 0) == sp.SP_ENOMEM
