@@ -31,35 +31,39 @@ def _f64(a) -> np.ndarray:
     return a.astype(np.float64)
 
 
-def lookahead_rows(Q_la, K_la, l: int, h: int, G: int) -> np.ndarray:
-    """Causal look-ahead logits u[j, k] = Q_la[j,l,h] . K_la[l,g,k] / sqrt(d), k <= j.
+def lookahead_rows(Q_la, K_la, l: int, h: int, G: int, shift: int = 0) -> np.ndarray:
+    """Causal look-ahead logits u[j, k] = Q_la[j,l,h] . K_la[l,g,k] / sqrt(d), k <= j - shift.
 
-    Entries with k > j are -inf (look-ahead step j has not seen later steps).
+    Entries with k > j - shift are -inf (row j has not seen later steps).
+    shift = 1 is the capture with the prompt's last query as row 0 (it sees
+    no look-ahead key) followed by the decode steps (row j sees keys 0..j-1).
     """
-    N, d = Q_la.shape[0], Q_la.shape[3]
+    d = Q_la.shape[3]
     g = h // G
-    q = _f64(Q_la[:, l, h, :])                      # [N, d]
-    kla = _f64(K_la[l, g])                          # [N, d]
-    u = (q @ kla.T) / math.sqrt(d)                  # [N, N]
-    u[np.triu_indices(N, k=1)] = -np.inf
+    q = _f64(Q_la[:, l, h, :])                      # [N_rows, d]
+    kla = _f64(K_la[l, g])                          # [N_la, d]
+    u = (q @ kla.T) / math.sqrt(d)                  # [N_rows, N_la]
+    for j in range(u.shape[0]):
+        u[j, max(0, j - shift + 1):] = -np.inf
     return u
 
 
-def _softmax_rows(s: np.ndarray, u: np.ndarray):
-    """Row-wise softmax over [prompt logits s[j] | look-ahead logits u[j, :j+1]]."""
+def _softmax_rows(s: np.ndarray, u: np.ndarray, shift: int = 0):
+    """Row-wise softmax over [prompt logits s[j] | look-ahead logits u[j, :j-shift+1]]."""
     N = s.shape[0]
     a = np.empty_like(s)
     a_la = np.zeros_like(u)
     for j in range(N):
-        row = np.concatenate([s[j], u[j, :j + 1]])
+        nl = max(0, j - shift + 1)
+        row = np.concatenate([s[j], u[j, :nl]])
         m = row.max()
         lse = m + math.log(np.exp(row - m).sum())
         a[j] = np.exp(s[j] - lse)
-        a_la[j, :j + 1] = np.exp(u[j, :j + 1] - lse)
+        a_la[j, :nl] = np.exp(u[j, :nl] - lse)
     return a, a_la
 
 
-def attention_rows(Q_la, K_prompt, K_la, l: int, h: int, k64=None):
+def attention_rows(Q_la, K_prompt, K_la, l: int, h: int, k64=None, shift: int = 0):
     """Post-softmax attention of every look-ahead query of (layer l, head h).
 
     Returns (a[N, M], a_la[N, N]): a[j, i] is the weight of prompt token i and
@@ -73,16 +77,19 @@ def attention_rows(Q_la, K_prompt, K_la, l: int, h: int, k64=None):
     q = _f64(Q_la[:, l, h, :])                      # [N, d]
     k = _f64(K_prompt[l, g]) if k64 is None else k64   # [M, d]
     s = (q @ k.T) / math.sqrt(d)                    # [N, M] prompt logits
-    u = lookahead_rows(Q_la, K_la, l, h, G)         # [N, N] look-ahead logits
-    return _softmax_rows(s, u)
+    u = lookahead_rows(Q_la, K_la, l, h, G, shift)  # [N, N_la] look-ahead logits
+    return _softmax_rows(s, u, shift)
 
 
-def importance(Q_la, K_prompt, K_la) -> np.ndarray:
+def importance(Q_la, K_prompt, K_la, shift: int = 0) -> np.ndarray:
     """importance_i = (1/N) sum_j max_{l,h} a[l,h,j,i]   (fp64, shape [M]).
 
-    Q_la[N, L, H, d], K_prompt[L, H_kv, M, d], K_la[L, H_kv, N, d].  With N = 0
-    every token gets importance 1.0 (compute_imp's fallback when no step was
-    captured).
+    Q_la[N, L, H, d], K_prompt[L, H_kv, M, d], K_la[L, H_kv, N - shift, d].
+    shift = 1: row 0 is the prompt's last query captured at prefill (its
+    softmax covers only the prompt keys), rows 1..N-1 the decode steps (the
+    llama.cpp guide captures the prefill's last row and then the decode
+    steps).  With N = 0 every token gets importance 1.0 (compute_imp's
+    fallback when no step was captured).
     """
     N, L, H, d = Q_la.shape
     H_kv, M = K_prompt.shape[1], K_prompt.shape[2]
@@ -94,7 +101,7 @@ def importance(Q_la, K_prompt, K_la) -> np.ndarray:
         for g in range(H_kv):
             k64 = _f64(K_prompt[l, g])
             for h in range(g * G, (g + 1) * G):
-                a, _ = attention_rows(Q_la, K_prompt, K_la, l, h, k64=k64)
+                a, _ = attention_rows(Q_la, K_prompt, K_la, l, h, k64=k64, shift=shift)
                 np.maximum(best, a, out=best)
     total = np.zeros(M, dtype=np.float64)
     for j in range(N):                              # mean over look-ahead steps, j in order
@@ -102,7 +109,7 @@ def importance(Q_la, K_prompt, K_la) -> np.ndarray:
     return total / N
 
 
-def row_lse(Q_la, K_prompt, K_la) -> np.ndarray:
+def row_lse(Q_la, K_prompt, K_la, shift: int = 0) -> np.ndarray:
     """lse[l, h, j] = log(sum_i exp(s[l,h,j,i]) + sum_{k<=j} exp(u[l,h,j,k]))  (fp64, [L, H, N]).
 
     The normaliser of look-ahead query j's softmax over the M prompt keys and
@@ -119,9 +126,9 @@ def row_lse(Q_la, K_prompt, K_la) -> np.ndarray:
             for h in range(g * G, (g + 1) * G):
                 q = _f64(Q_la[:, l, h, :])
                 s = (q @ k.T) / math.sqrt(d)
-                u = lookahead_rows(Q_la, K_la, l, h, G)
+                u = lookahead_rows(Q_la, K_la, l, h, G, shift)
                 for j in range(N):
-                    row = np.concatenate([s[j], u[j, :j + 1]])
+                    row = np.concatenate([s[j], u[j, :max(0, j - shift + 1)]])
                     m = row.max()
                     out[l, h, j] = m + math.log(np.exp(row - m).sum())
     return out
