@@ -124,6 +124,24 @@ sp_status sp_score(const void* Q_la, const void* K_prompt, const void* K_la,
                    int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype,
                    float* importance, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes sp_score_prefill needs (N = decode steps; 0 if the shape is invalid). */
+size_t sp_score_prefill_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype);
+
+/* sp_score for the capture the llama.cpp guide makes ("How It Works": the
+ * prefill's last row, then the look-ahead decode steps): N + 1 query rows,
+ * where row 0 is the prompt's last query at prefill -- its softmax covers only
+ * the M prompt keys -- and row j >= 1 is decode step j - 1, whose softmax also
+ * covers look-ahead keys 0..j-1.  importance[i] = (1/(N+1)) sum_j max_{l,h} a[l,h,j,i].
+ *
+ *   Q_rows    [N + 1, L, H, d]  row 0: the prompt's last query; rows 1..N: decode queries
+ *   K_prompt  [L, H_kv, M, d]
+ *   K_la      [L, H_kv, N, d]   the decode steps' keys (may be NULL when N == 0)
+ *
+ * Requirements as sp_score with N + 1 rows ((N + 1) * (H / H_kv) <= 256). */
+sp_status sp_score_prefill(const void* Q_rows, const void* K_prompt, const void* K_la,
+                           int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype,
+                           float* importance, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes sp_score_lse needs for this shape (0 if the shape is invalid). */
 size_t sp_score_lse_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype);
 

@@ -18,12 +18,13 @@ __all__ = [
     "SP_OK", "SP_EINVAL", "SP_ENOMEM", "SP_ECUDA", "SP_EDEVICE", "SP_ETIMEOUT", "SP_EUNSUPPORTED",
     "SP_BF16", "SP_F32", "SP_SELECT_TOPK", "SP_SELECT_MASS", "SpBoost", "SpError", "lib", "lib_path",
     "sp_score_workspace_size", "sp_score", "sp_score_lse_workspace_size", "sp_score_lse",
+    "sp_score_prefill_workspace_size", "sp_score_prefill",
     "sp_score_varlen_workspace_size", "sp_score_varlen",
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
     "sp_select_noalloc", "sp_select_rules_workspace_size", "sp_select_rules", "SpKeepRules", "GUIDE_RULES",
     "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
     "sp_kernel_launches",
-    "score", "score_lse", "score_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
+    "score", "score_lse", "score_prefill", "score_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
 ]
 
 SP_OK, SP_EINVAL, SP_ENOMEM, SP_ECUDA, SP_EDEVICE, SP_ETIMEOUT, SP_EUNSUPPORTED = range(7)
@@ -67,6 +68,8 @@ _SIGS = {
     "sp_score_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i64, _i32, _i32]),
     "sp_score": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _sz, _vp]),
     "sp_score_lse_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i64, _i32, _i32]),
+    "sp_score_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i64, _i32, _i32]),
+    "sp_score_prefill": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _sz, _vp]),
     "sp_score_lse": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _sz, _vp]),
     "sp_score_varlen_workspace_size": (_sz, [_i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32]),
     "sp_score_varlen": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
@@ -153,6 +156,16 @@ def sp_score_workspace_size(L, H, H_kv, d, M, N, dtype) -> int:
 def sp_score(Q_la, K_prompt, K_la, L, H, H_kv, d, M, N, dtype, importance, ws, ws_bytes, stream=None) -> int:
     return lib().sp_score(_ptr(Q_la), _ptr(K_prompt), _ptr(K_la), L, H, H_kv, d, M, N, dtype,
                           _ptr(importance), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def sp_score_prefill_workspace_size(L, H, H_kv, d, M, N, dtype) -> int:
+    return lib().sp_score_prefill_workspace_size(L, H, H_kv, d, M, N, dtype)
+
+
+def sp_score_prefill(Q_rows, K_prompt, K_la, L, H, H_kv, d, M, N, dtype, importance, ws, ws_bytes,
+                     stream=None) -> int:
+    return lib().sp_score_prefill(_ptr(Q_rows), _ptr(K_prompt), _ptr(K_la), L, H, H_kv, d, M, N, dtype,
+                                  _ptr(importance), _ptr(ws), ws_bytes, _stream(stream))
 
 
 def sp_score_lse_workspace_size(L, H, H_kv, d, M, N, dtype) -> int:
@@ -294,6 +307,23 @@ def score(Q_la, K_prompt, K_la, *, importance=None, ws=None, stream=None, check=
     need = sp_score_workspace_size(L, H, H_kv, d, M, N, dt)
     ws = _workspace(need, K_prompt.device, ws)
     _check(sp_score(Q_la, K_prompt, K_la, L, H, H_kv, d, M, N, dt, importance, ws, ws.numel(), stream))
+    _check_device(ws, stream, check)
+    return importance
+
+
+def score_prefill(Q_rows, K_prompt, K_la, *, importance=None, ws=None, stream=None, check=False):
+    """Importance [M] (fp32) from the prefill's last query (Q_rows[0]) and N decode steps (Q_rows[1:]):
+    Q_rows [N+1,L,H,d], K_prompt [L,H_kv,M,d], K_la [L,H_kv,N,d]."""
+    import torch
+    N1, L, H, d = Q_rows.shape
+    _, H_kv, M, _ = K_prompt.shape
+    dt = _dtype_code(K_prompt)
+    if importance is None:
+        importance = torch.empty(M, dtype=torch.float32, device=K_prompt.device)
+    need = sp_score_prefill_workspace_size(L, H, H_kv, d, M, N1 - 1, dt)
+    ws = _workspace(need, K_prompt.device, ws)
+    _check(sp_score_prefill(Q_rows, K_prompt, K_la, L, H, H_kv, d, M, N1 - 1, dt, importance, ws, ws.numel(),
+                            stream))
     _check_device(ws, stream, check)
     return importance
 

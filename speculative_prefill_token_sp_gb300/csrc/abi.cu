@@ -115,6 +115,7 @@ ScoreProblem make_score_problem(const void* Q, const void* K, const void* Kla, i
     p.Q = Q; p.K = K; p.Kla = Kla; p.importance = imp; p.cu_M_host = cu;
     p.lse_in = nullptr;
     p.lse_mode = false;
+    p.la_shift = 0;
     p.B = B; p.L = L; p.H = H; p.H_kv = H_kv; p.d = d; p.N = N; p.dtype = dtype;
     p.T = cu[B];
     p.max_M = 0;
@@ -132,11 +133,12 @@ sp_status run_score(const char* fn, const ScoreProblem& p, void* ws, size_t ws_b
     const size_t need = score_ws(p);
     if (p.T > 0 && p.N > 0) {
         const void* third = p.lse_mode ? static_cast<const void*>(p.lse_in) : p.Kla;
-        if (!p.Q || !p.K || !third) {
+        const bool third_needed = p.lse_mode || p.N > p.la_shift;     // look-ahead keys exist
+        if (!p.Q || !p.K || (third_needed && !third)) {
             set_error("%s: null input pointer", fn);
             return SP_EINVAL;
         }
-        if (!aligned16(p.Q) || !aligned16(p.K) || (!p.lse_mode && !aligned16(p.Kla)) ||
+        if (!aligned16(p.Q) || !aligned16(p.K) || (!p.lse_mode && third_needed && !aligned16(p.Kla)) ||
             (p.lse_mode && reinterpret_cast<uintptr_t>(p.lse_in) % 4 != 0)) {
             set_error("%s: input pointers must be 16-byte aligned (lse: 4-byte)", fn);
             return SP_EINVAL;
@@ -283,6 +285,34 @@ sp_status sp_score(const void* Q_la, const void* K_prompt, const void* K_la, int
     int64_t cu[2] = {0, M};
     ScoreProblem p = make_score_problem(Q_la, K_prompt, K_la, 1, cu, L, H, H_kv, d, N, dtype, importance);
     return run_score("sp_score", p, ws, ws_bytes, stream);
+}
+
+size_t sp_score_prefill_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype) {
+    if (M < 0 || N < 0 || check_shape("sp_score_prefill_workspace_size", L, H, H_kv, d, N + 1, dtype) != SP_OK)
+        return 0;
+    int64_t cu[2] = {0, M};
+    ScoreProblem p = make_score_problem(nullptr, nullptr, nullptr, 1, cu, L, H, H_kv, d, N + 1, dtype, nullptr);
+    p.la_shift = 1;
+    return score_ws(p);
+}
+
+sp_status sp_score_prefill(const void* Q_rows, const void* K_prompt, const void* K_la, int L, int H, int H_kv,
+                           int d, int64_t M, int N, sp_dtype dtype, float* importance, void* ws,
+                           size_t ws_bytes, void* stream) {
+    if (N < 0) {
+        set_error("sp_score_prefill: N (decode steps) must be >= 0 (got %d)", N);
+        return SP_EINVAL;
+    }
+    sp_status s = check_shape("sp_score_prefill", L, H, H_kv, d, N + 1, dtype);
+    if (s != SP_OK) return s;
+    if (M < 0 || M > (int64_t)INT32_MAX) {
+        set_error("sp_score_prefill: M must be in [0, 2^31-1] (got %lld)", (long long)M);
+        return M < 0 ? SP_EINVAL : SP_EUNSUPPORTED;
+    }
+    int64_t cu[2] = {0, M};
+    ScoreProblem p = make_score_problem(Q_rows, K_prompt, K_la, 1, cu, L, H, H_kv, d, N + 1, dtype, importance);
+    p.la_shift = 1;
+    return run_score("sp_score_prefill", p, ws, ws_bytes, stream);
 }
 
 size_t sp_score_lse_workspace_size(int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype) {

@@ -32,6 +32,7 @@ constexpr int kMaxBatch = 256;
 
 struct Geo {
     int B, L, H, H_kv, G, d, N, R;
+    int la_shift, N_la;             // row j sees look-ahead keys 0..j-la_shift of N_la
     int RB, n_rb, tpr, dpad, max_splits;
     int64_t T;
     float scale;
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Geo geo, const 
         }
         const int j = r / geo.G, h = g * geo.G + r % geo.G;
         const In* q = Q + ((((int64_t)b * geo.N + j) * geo.L + l) * geo.H + h) * geo.d;
-        for (int k = 0; k <= j; ++k) {
-            const In* kk = Kla + ((((int64_t)b * geo.L + l) * geo.H_kv + g) * geo.N + k) * geo.d;
+        for (int k = 0; k <= j - geo.la_shift; ++k) {
+            const In* kk = Kla + ((((int64_t)b * geo.L + l) * geo.H_kv + g) * geo.N_la + k) * geo.d;
             float u = 0.f;
             for (int t = 0; t < geo.d; ++t) u = fmaf(to_f(q[t]), to_f(kk[t]), u);
             merge(m, z, u * geo.scale, 1.f);
@@ -274,6 +275,7 @@ int pow2_at_least(int x) { int p = 1; while (p < x) p <<= 1; return p; }
 bool make_geo(const ScoreProblem& p, Geo& g) {
     if (p.B > kMaxBatch) return false;
     g.B = p.B; g.L = p.L; g.H = p.H; g.H_kv = p.H_kv; g.G = p.H / p.H_kv; g.d = p.d; g.N = p.N;
+    g.la_shift = p.la_shift; g.N_la = p.N - p.la_shift;
     g.R = p.N * g.G;
     g.RB = std::min(g.R, (kRowsMax / g.G) * g.G);
     if (g.RB < 1) g.RB = g.G;          // G > 64: one look-ahead step per CTA

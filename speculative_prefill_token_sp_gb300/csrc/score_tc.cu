@@ -108,6 +108,7 @@ struct TcParams {
     int64_t tok0;       // row of the prompt's first token within a slab (its offset in the pack)
     int first;          // 1 for the call's first prompt: its preparation clears the status
     int lse_mode;       // 1: each row's lse is given (lse_in); no statistics pass, no exchange
+    int la_shift;       // row j sees look-ahead keys 0..j - la_shift
     const float* lse_in;  // [L, H, N] natural-log softmax normalisers (lse_mode)
     float scale, scale_log2e;
     // shared-memory carve (byte offsets from the 1024-aligned base)
@@ -417,8 +418,8 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
         if (r < p.R) {
             const int j = r / p.G, h = g * p.G + r % p.G;
             const __nv_bfloat16* q = Q + (((size_t)j * p.L + l) * p.H + h) * p.d;
-            for (int k = 0; k <= j; ++k) {
-                const __nv_bfloat16* kk = Kla + (((size_t)l * p.H_kv + g) * p.N + k) * p.d;
+            for (int k = 0; k <= j - p.la_shift; ++k) {
+                const __nv_bfloat16* kk = Kla + (((size_t)l * p.H_kv + g) * (p.N - p.la_shift) + k) * p.d;
                 float u = 0.f;
                 for (int t = lane; t < p.d; t += 32) u = fmaf(__bfloat162float(q[t]), __bfloat162float(kk[t]), u);
 #pragma unroll
@@ -1034,6 +1035,7 @@ bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
     p.tiles_per_group = (p.n_tiles_max + 1) / 2;
     const int slab_cols = p.tiles_per_group * 16;
     p.lse_mode = q.lse_mode ? 1 : 0;
+    p.la_shift = q.la_shift;
     p.lse_in = q.lse_in;
     if (p.lse_mode) {
         // no held logits: all of TMEM holds landing tiles
@@ -1186,7 +1188,9 @@ static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const C
     p.acc_glob = reinterpret_cast<unsigned*>(w + plan.off_acc_glob);
     p.arrivals = reinterpret_cast<int*>(w + plan.off_arrivals);
     const __nv_bfloat16* Qb = static_cast<const __nv_bfloat16*>(q.Q) + (size_t)b * q.N * q.L * q.H * q.d;
-    const __nv_bfloat16* Klab = static_cast<const __nv_bfloat16*>(q.Kla) + (size_t)b * q.L * q.H_kv * q.N * q.d;
+    const __nv_bfloat16* Klab = q.Kla ? static_cast<const __nv_bfloat16*>(q.Kla) +
+                                            (size_t)b * q.L * q.H_kv * (q.N - q.la_shift) * q.d
+                                      : nullptr;
     tc_prep_kernel<<<p.S, 256, 0, st>>>(p, Qb, Klab, w + plan.off_qimg, reinterpret_cast<float2*>(w + plan.off_la),
                                         p.lse, p.partials, p.hdr);
     SP_LAUNCH_CHECK();

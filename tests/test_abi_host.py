@@ -142,3 +142,13 @@ def test_select_rules_validation(sp):
     assert f(16, 512, 32, 3, 0, 0.3, None, (128, 1, -5), 16, 16, 16, need, 0) == sp.SP_EINVAL
     assert f(16, 512, 32, 3, 0, 0.3, None, (5000, 1, 0), 16, 16, 16, need, 0) == sp.SP_EUNSUPPORTED
     assert f(16, 512, 32, 3, 0, 0.3, None, sp.GUIDE_RULES, 16, 16, 16, need - 1, 0) == sp.SP_ENOMEM
+
+
+def test_score_prefill_validation(sp):
+    need = sp.sp_score_prefill_workspace_size(2, 4, 2, 64, 512, 3, sp.SP_F32)
+    assert need > 0
+    f = sp.sp_score_prefill
+    assert f(16, 16, 16, 2, 4, 2, 64, 512, -1, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL       # N < 0
+    assert f(16, 16, 16, 2, 4, 2, 64, 512, 200, sp.SP_F32, 16, 16, need, 0) == sp.SP_EUNSUPPORTED  # (N+1)*G > 256
+    assert f(16, 16, 16, 2, 4, 2, 64, 512, 3, sp.SP_F32, 16, 16, need - 1, 0) == sp.SP_ENOMEM
+    assert f(16, 16, None, 2, 4, 2, 64, 512, 3, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL       # keys needed
