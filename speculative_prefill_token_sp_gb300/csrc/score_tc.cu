@@ -28,10 +28,11 @@
 //    tile) and one half of the query rows, and works on it alone: its hand-offs
 //    are mbarriers that count the warps taking part, never a barrier with
 //    another warp.  P1 reads its part of a landing tile, frees it at once,
-//    reduces per-row softmax statistics (max, sum of exp) over its 32 tokens
-//    through a warp-private transpose, and stores the part again in the group's
-//    "held" TMEM region as fp16 offsets from the quadrant's row maxima (half the
-//    columns, so many more slabs fit).  P2 reads the held part, subtracts lse,
+//    adds each row's exp(s - c) over its 32 tokens to the row's running sum
+//    (shuffle butterflies, no shared memory), c being a per-row reference the
+//    warp keeps for the slab, and stores the part again in the group's "held"
+//    TMEM region as fp16 offsets s - c (half the columns, so many more slabs
+//    fit).  P2 reads the held part, subtracts lse,
 //    takes the max over the G heads of each look-ahead step and folds it into a
 //    per-token running max in shared memory.  Held slabs never block the MMA
 //    warp, so the HBM stream does not wait for the lse exchange;
@@ -46,10 +47,12 @@
 //    them into a shared-memory ring for the epilogue.
 //
 // Precision: P1 statistics use the fp32 logits.  P2 reads w = s - c in fp16,
-// c = the row maximum over the warp's 32 tokens of the tile, so w <= 0 and its
-// rounding error is at most |w| * 2^-11 (fp16 unit roundoff): a weight
-// exp(w + c - lse) <= exp(w) is off by at most |w| * 2^-11 relative (< 1% for
-// w > -20) and by < 1.8e-4 absolute (the maximum of exp(w) * |w| * 2^-11).
+// c = the largest logit of the row seen so far in the slab by the warp (taken
+// again whenever a value exceeds it by more than kRefMargin = 2), so w <= 2
+// and its rounding error is at most |w| * 2^-11 (fp16 unit roundoff).  A
+// weight exp(w + c - lse) is then off by at most |w| * 2^-11 relative: < 1e-3
+// for 0 < w <= 2, < 1% for -20 < w <= 0, and for w <= 0 by < 1.8e-4 absolute
+// (c <= lse, and exp(w) * |w| * 2^-11 peaks at w = -1).
 //
 // Every wait is bounded: on timeout the kernel records SP_ETIMEOUT in the
 // workspace header, all roles stop, in-flight copies and MMAs are waited for
@@ -77,6 +80,11 @@ constexpr int kUnit = 32;            // token-range granularity
 constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 8;         // tiles per CTA per slab
+// How far (natural-log units) a logit may rise above its row's reference
+// before the epilogue retakes the reference: fp16 offsets below 2 keep the
+// dominant values of a row to 2^-11 relative.
+constexpr float kRefMargin = 2.0f;
+constexpr int kRefBytes = 16 * 16 * 4;  // 16 row references per epilogue warp
 constexpr int kMaxHeld = 12;         // held slabs per epilogue group
 constexpr int kRing = 16;            // entries of the lse ring
 constexpr int kStatsRing = 4;        // entries of the statistics ring
@@ -112,7 +120,7 @@ struct TcParams {
     const float* lse_in;  // [L, H, N] natural-log softmax normalisers (lse_mode)
     float scale, scale_log2e;
     // shared-memory carve (byte offsets from the 1024-aligned base)
-    int off_q, off_s, off_acc, off_c, off_stats, off_lse, off_bar, smem_bytes;
+    int off_q, off_acc, off_c, off_ref, off_stats, off_lse, off_bar, smem_bytes;
     // workspace
     const uint8_t* qimg;            // [S][kRP * d] bf16, 128B-swizzled image of the slab's query rows
     const float2* la;               // [S][kRP] softmax statistics of the look-ahead keys
@@ -339,6 +347,51 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
         : "memory");
 }
 
+// 16 consecutive floats from a 16-byte aligned shared-memory address.
+__device__ __forceinline__ void load16(const float* src, float (&v)[16]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 f = reinterpret_cast<const float4*>(src)[k];
+        v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
+    }
+}
+
+// Row results of 16 values per lane over the warp's 32 lanes (maximum or sum)
+// by a halving butterfly: on return lanes 2r and 2r + 1 hold row r's.  A lane
+// with `take` false contributes -inf (maximum) or 0 (sum).
+template <bool kMax>
+__device__ __forceinline__ float warp_rows16(const float (&v)[16], bool take) {
+    const int lane = threadIdx.x & 31;
+    auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+    const float none = kMax ? -INFINITY : 0.f;
+    float a8[8], a4[4], a2[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float lo = take ? v[k] : none, hi = take ? v[k + 8] : none;
+        a8[k] = op(b4 ? hi : lo, __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        a4[k] = op(b3 ? a8[k + 4] : a8[k], __shfl_xor_sync(0xffffffffu, b3 ? a8[k] : a8[k + 4], 8));
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        a2[k] = op(b2 ? a4[k + 2] : a4[k], __shfl_xor_sync(0xffffffffu, b2 ? a4[k] : a4[k + 2], 4));
+    float a1 = op(b1 ? a2[1] : a2[0], __shfl_xor_sync(0xffffffffu, b1 ? a2[0] : a2[1], 2));
+    return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+}
+
+// A token's running maxima of the look-ahead steps rh*(16/G) .. + 16/G - 1
+// (steps past N read as 0, never used).
+template <int G>
+__device__ __forceinline__ void load_acc(const float* a, int rh, int N, float (&v)[16 / G]) {
+#pragma unroll
+    for (int jl = 0; jl < 16 / G; ++jl) {
+        const int jj = rh * (16 / G) + jl;
+        v[jl] = jj < N ? a[jj * kTileRows] : 0.f;
+    }
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Order-preserving 32-bit code of a float (a < b  <=>  code(a) < code(b) as
@@ -471,9 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
     uint8_t* k_stage = smem;                                       // [stages][kStageBytes]
     uint8_t* q_buf = smem + p.off_q;                               // [nq][kQBytes]
-    float* wbuf = reinterpret_cast<float*>(smem + p.off_s);        // [16 epilogue warps][16][33]
     float* acc = reinterpret_cast<float*>(smem + p.off_acc);       // [2 groups][n_tiles_max][N][128]
     float* cbuf = reinterpret_cast<float*>(smem + p.off_c);        // [2 groups][held][tiles_per_group][4][kRP]
+    float* rbuf = reinterpret_cast<float*>(smem + p.off_ref);      // [16 epilogue warps][16]
     float2* stats = reinterpret_cast<float2*>(smem + p.off_stats); // [kStatsRing][2 groups][4][kRP]
     float* lse_ring = reinterpret_cast<float*>(smem + p.off_lse);  // [kRing][kRP]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
@@ -627,15 +680,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         const int quad = warp & 3;                     // TMEM lane quadrant of this warp
         const int rh = (ew >> 2) & 1;                  // query rows rh*16 .. rh*16 + 15
         const int tok = quad * 32 + lane;              // token row inside a tile
-        const int row = lane & 15, th = lane >> 4;     // reduction role: row, 16-token half
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
         const int tpg = p.tiles_per_group;             // held tile slots per slab
-        float* wp = wbuf + ew * (16 * 33);             // this warp's transpose buffer
         float* acc_g = acc + (size_t)grp * p.n_tiles_max * p.N * kTileRows;
         float* cb_g = cbuf + (size_t)grp * p.held * tpg * 4 * kRP;
+        float* wref = rbuf + ew * 16;                  // the warp's 16 row references (P1)
         const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * tpg * 16 + rh * 8);
         const int odd = n_tiles & 1;
         int lt = 0;                                    // landing tiles consumed so far
+        uint32_t chg = 0;                              // held tiles (hs * tpg + j) whose references P2 reloads
         bool ok = true;
         if (p.lse_mode) {
             // lse given: one pass, exp(s - lse) straight from the landing tiles
@@ -686,11 +739,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     ok = false;
                     break;
                 }
-                // lanes row and row + 16: running statistics of query row rh*16 + row
-                // over this quadrant's tokens (same m_run in both, z_run per half)
-                float m_run = -INFINITY, z_run = 0.f;
+                // Statistics of query row rh*16 + r over this quadrant's tokens,
+                // relative to a reference ref[r] that the whole warp shares: each
+                // tile's exp(s - ref) are summed over the 32 lanes and added to
+                // the row's running sum (lanes 2r, 2r + 1).  The reference starts at
+                // the row's maximum over the slab's first tile with a valid token
+                // and rises to a tile's maximum whenever a logit exceeds it by more
+                // than kRefMargin (the sums so far are then rescaled).  It is
+                // always a logit of the row, so z >= 1 once a token was valid, and
+                // the held fp16 offsets s - ref stay at most kRefMargin above 0.
+                // Row maxima and sums go through a shuffle butterfly, and a tile's
+                // references are stored for P2 only when they change: shared
+                // memory is slow while the MMA reads its operands.
+                float ref_lane = 0.f;                  // ref of row rh*16 + (lane >> 1); all 16 in wref
+                float z_lane = 0.f;                    // and that row's sum of exp(s - ref)
+                bool have_ref = false;
+                chg &= ~(((1u << tpg) - 1u) << (hs * tpg));
                 for (int t = t0, j = 0; t < n_tiles; t += 2, ++j, ++lt) {
                     const int slot = grp * p.land + lt % p.land;
+                    float ref[16];                     // read while the landing tile is awaited
+                    if (have_ref) {
+                        load16(wref, ref);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) ref[r] = 0.f;
+                    }
                     if (!warp_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6)) {
                         ok = false;
                         break;
@@ -702,45 +775,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));    // this part is read
                     const bool valid = t * kTileRows + tok < len;
+                    float o[16];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) wp[r * 33 + lane] = valid ? x[r] : -INFINITY;
-                    __syncwarp();
-                    float v[16];
+                    for (int r = 0; r < 16; ++r) o[r] = fmaf(x[r], p.scale, -ref[r]);
+                    bool redo;
+                    if (have_ref) {
+                        float om[4] = {o[0], o[1], o[2], o[3]};
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = wp[row * 33 + th * 16 + k];
-                    float mq[4] = {v[0], v[1], v[2], v[3]};
-#pragma unroll
-                    for (int k = 4; k < 16; ++k) mq[k & 3] = fmaxf(mq[k & 3], v[k]);
-                    float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_t = mx == -INFINITY ? -INFINITY : mx * p.scale;
-                    const float m_new = fmaxf(m_run, m_t);
-                    if (m_new != -INFINITY) {
-                        const float off = m_new * 1.4426950408889634f;
-                        float zq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) zq[k & 3] += ex2_approx(fmaf(v[k], p.scale_log2e, -off));
-                        const float zt = (zq[0] + zq[1]) + (zq[2] + zq[3]);
-                        z_run = (m_run == -INFINITY ? 0.f : z_run * ex2_approx((m_run - m_new) * 1.4426950408889634f)) + zt;
-                        m_run = m_new;
+                        for (int k = 4; k < 16; ++k) om[k & 3] = fmaxf(om[k & 3], o[k]);
+                        redo = __any_sync(0xffffffffu, valid && fmaxf(fmaxf(om[0], om[1]), fmaxf(om[2], om[3])) > kRefMargin);
+                    } else {
+                        redo = __any_sync(0xffffffffu, valid);
                     }
-                    // the quadrant's row maxima are the fp16 references of its held copy
-                    float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
-                    if (th == 0) cq[row] = m_t == -INFINITY ? 0.f : m_t;
-                    __syncwarp();
+                    if (redo) {
+                        // each reference rises by its row's largest offset (or starts at it)
+                        const float mx = warp_rows16<true>(o, valid);   // finite: a lane is valid
+                        const float dm = have_ref ? fmaxf(mx, 0.f) : mx;
+                        ref_lane += dm;
+                        z_lane = have_ref ? z_lane * ex2_approx(-dm * 1.4426950408889634f) : 0.f;
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) o[r] -= __shfl_sync(0xffffffffu, dm, 2 * r);
+                        if ((lane & 1) == 0) wref[lane >> 1] = ref_lane;
+                        __syncwarp();
+                        have_ref = true;
+                    }
+                    if (have_ref) {
+                        float e[16];
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) e[r] = ex2_approx(o[r] * 1.4426950408889634f);
+                        z_lane += warp_rows16<false>(e, valid);
+                    }
                     uint32_t pk[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const __half2 h2 = __floats2half2_rn(fmaf(x[2 * k], p.scale, -cq[2 * k]),
-                                                             fmaf(x[2 * k + 1], p.scale, -cq[2 * k + 1]));
+                        const __half2 h2 = __floats2half2_rn(o[2 * k], o[2 * k + 1]);
                         pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    if (j == 0 || redo) {
+                        // the tile's fp16 references differ from the previous tile's: P2 reloads them
+                        const float rr = __shfl_sync(0xffffffffu, ref_lane, 2 * (lane & 15));
+                        float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
+                        if (lane < 16) cq[lane] = rr;
+                        chg |= 1u << (hs * tpg + j);
                     }
                     tmem_st8(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
                     tmem_wait_st();
                 }
                 if (!ok) break;
-                const float z = z_run + __shfl_xor_sync(0xffffffffu, z_run, 16);
-                if (th == 0) stats[((q * 2 + grp) * 4 + quad) * kRP + rh * 16 + row] = make_float2(m_run, z);
+                if ((lane & 1) == 0)
+                    stats[((q * 2 + grp) * 4 + quad) * kRP + rh * 16 + (lane >> 1)] =
+                        make_float2(have_ref ? ref_lane : -INFINITY, z_lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&stats_full[q]));
             }
@@ -752,25 +836,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     ok = false;
                     break;
                 }
-                float lr[16];
+                const float* lq = lse_ring + q * kRP + rh * 16;   // the slot is held until P2 is done
+                float d[16];                           // the tile's reference - lse, per row
 #pragma unroll
-                for (int r = 0; r < 16; ++r) lr[r] = lse_ring[q * kRP + rh * 16 + r];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&lse_empty[q]));
+                for (int r = 0; r < 16; ++r) d[r] = 0.f;
                 for (int t = t0, j = 0; t < n_tiles; t += 2, ++j) {
                     uint32_t pk[8];
                     tmem_ld8_issue(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
+                    // shared-memory reads overlap the TMEM load
+                    float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
+                    float av[16 / G];
+                    load_acc<G>(a, rh, p.N, av);
+                    if ((chg >> (hs * tpg + j)) & 1u) {
+                        float c[16], l[16];
+                        load16(cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16, c);
+                        load16(lq, l);
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) d[r] = c[r] - l[r];
+                    }
                     tmem_ld8_wait(pk);
-                    const float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
                     float y[16];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
-                        y[2 * k] = f.x + (cq[2 * k] - lr[2 * k]);
-                        y[2 * k + 1] = f.y + (cq[2 * k + 1] - lr[2 * k + 1]);
+                        y[2 * k] = f.x + d[2 * k];
+                        y[2 * k + 1] = f.y + d[2 * k + 1];
                     }
                     // rows rh*16 + k are look-ahead steps jj = rh*(16/G) + k/G, heads k%G
-                    float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
 #pragma unroll
                     for (int jl = 0; jl < 16 / G; ++jl) {
                         const int jj = rh * (16 / G) + jl;
@@ -778,10 +870,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                             float m = y[jl * G];
 #pragma unroll
                             for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jl * G + hh]);
-                            a[jj * kTileRows] = fmaxf(a[jj * kTileRows], m);
+                            a[jj * kTileRows] = fmaxf(av[jl], m);
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&lse_empty[q]));
             }
         }
         epi_sync();                                    // both groups' running maxima are complete
@@ -1055,16 +1149,16 @@ bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
     }
     p.held_base = 2 * p.land * kRP;               // after both groups' landing tiles
     if (p.held_base + 2 * p.held * slab_cols > kTmemCols) return false;
+    if (p.held * p.tiles_per_group > 32) return false;   // one bit per held tile
     p.scale = 1.0f / sqrtf((float)q.d);
     p.scale_log2e = p.scale * 1.4426950408889634f;
     const int stage_bytes = kTileRows * q.d * 2;
     const int q_bytes = kRP * q.d * 2;
     const int n_bars = 2 * 8 + 2 * kMaxQ + 4 * kMaxLand + 2 * kStatsRing + 2 * kRing + 2;
-    const int w_bytes = 16 * 16 * 33 * 4;                   // transpose buffer per epilogue warp
     const int acc_bytes = 2 * p.n_tiles_max * p.N * kTileRows * 4;   // running max (one per group)
     const int c_bytes = 2 * p.held * p.tiles_per_group * 4 * kRP * 4;   // fp16 references per quadrant
     const int ring_bytes = kStatsRing * 2 * 4 * kRP * 8 + kRing * kRP * 4;
-    const int fixed = w_bytes + acc_bytes + c_bytes + ring_bytes + 16 + n_bars * 8 + 16 + 1024;
+    const int fixed = kRefBytes + acc_bytes + c_bytes + ring_bytes + 16 + n_bars * 8 + 16 + 1024;
     // query images: the TMA loads slab s's image once slab s - nq is done, so
     // with one or two tiles per slab a ring of four keeps it ahead of the K
     // stream; with more tiles two are enough
@@ -1078,12 +1172,12 @@ bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
     int off = p.stages * stage_bytes;
     p.off_q = off;
     off += p.nq * q_bytes;
-    p.off_s = off;
-    off += w_bytes;
     p.off_acc = off;
     off += acc_bytes;
     p.off_c = off;
     off += c_bytes;
+    p.off_ref = off;
+    off += kRefBytes;
     p.off_stats = off;
     off += kStatsRing * 2 * 4 * kRP * 8;
     p.off_lse = off;
