@@ -75,7 +75,7 @@ constexpr int kMergeBase = 608;      // warps 19-22: merge
 constexpr int kFetchWarp = 23;
 constexpr int kEpiWarpsPerGroup = 8;
 constexpr int kTileRows = 128;       // tokens per MMA tile (MMA M)
-constexpr int kBoxRows = 32;         // rows per TMA box
+constexpr int kBoxRows = 32;         // rows per TMA box of a slab's ragged last tile (full tiles: one box)
 constexpr int kUnit = 32;            // token-range granularity
 constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
@@ -190,8 +190,8 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
 // Every waiter consumes a barrier's phases in order, and the producer of phase
 // k + 1 first needs every waiter's hand-off of phase k, so a waiter is never
 // more than one phase ahead of the barrier.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
+                                            int where) {
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_suspend(bar, parity, 1000u)) return true;
@@ -202,6 +202,13 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
             return false;
         }
     }
+}
+
+// The common case (the phase already completed) stays inline: the single-lane
+// TMA and MMA issuers share their SM sub-partitions with busy epilogue warps.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
+                                          int where) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, hdr, where);
 }
 
 __device__ __forceinline__ unsigned long long ld_cg64(const unsigned long long* p) {
@@ -499,8 +506,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return ok != 0;
 }
 
+// K viewed as a 2D tensor of rows by d bf16 columns, in 64-column boxes of 128
+// rows (a full tile per copy) and of 32 rows (a slab's ragged last tile).
+struct KMaps {
+    CUtensorMap full, tail;
+};
+
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ KMaps kmaps,
                                                                 const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -592,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             int it = 0;
+            int st = 0, st_round = 0;          // it % stages, it / stages
             bool ok = true;
             for (int i = 0; i < n_slabs && ok; ++i) {
                 const int s = cf + i * p.F, qb = i % p.nq;
@@ -602,18 +616,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                           smem_u32(&q_full[qb]));
                 const int64_t row0 = (int64_t)s * p.slab_stride + p.tok0 + t_begin;
                 for (int t = 0; t < n_tiles; ++t, ++it) {
-                    const int st = it % p.stages;
-                    if (it >= p.stages)
-                        ok = mbar_wait(smem_u32(&k_empty[st]), ((it / p.stages) - 1) & 1, abort_flag, p.hdr, 2);
+                    if (st_round > 0)
+                        ok = mbar_wait(smem_u32(&k_empty[st]), (st_round - 1) & 1, abort_flag, p.hdr, 2);
                     if (!ok) break;
                     const int rows = min(kTileRows, len - t * kTileRows);
-                    const int nbox = (rows + kBoxRows - 1) / kBoxRows;
-                    mbar_expect_tx(smem_u32(&k_full[st]), (uint32_t)(nbox * kBoxRows * D * 2));
-                    uint8_t* dst = k_stage + (size_t)st * kStageBytes;
-                    for (int hf = 0; hf < kHalves; ++hf)
-                        for (int b = 0; b < nbox; ++b)
-                            tma_load_2d(smem_u32(dst + hf * (kTileRows * 128) + b * (kBoxRows * 128)), &kmap,
-                                        hf * 64, (int)(row0 + t * kTileRows + b * kBoxRows), smem_u32(&k_full[st]));
+                    const uint32_t dst = smem_u32(k_stage + (size_t)st * kStageBytes);
+                    const uint32_t bar = smem_u32(&k_full[st]);
+                    const int y = (int)(row0 + t * kTileRows);
+                    if (rows == kTileRows) {
+                        mbar_expect_tx(bar, (uint32_t)(kTileRows * D * 2));
+#pragma unroll
+                        for (int hf = 0; hf < kHalves; ++hf)
+                            tma_load_2d(dst + hf * (kTileRows * 128), &kmaps.full, hf * 64, y, bar);
+                    } else {
+                        const int nbox = (rows + kBoxRows - 1) / kBoxRows;
+                        mbar_expect_tx(bar, (uint32_t)(nbox * kBoxRows * D * 2));
+                        for (int hf = 0; hf < kHalves; ++hf)
+                            for (int b = 0; b < nbox; ++b)
+                                tma_load_2d(dst + hf * (kTileRows * 128) + b * (kBoxRows * 128), &kmaps.tail, hf * 64,
+                                            y + b * kBoxRows, bar);
+                    }
+                    if (++st == p.stages) {
+                        st = 0;
+                        ++st_round;
+                    }
                 }
             }
             // wait (bounded) for every copy still in flight before the CTA may exit
@@ -627,34 +653,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            int it = 0;
-            int lt0 = 0, lt1 = 0;          // landing tiles written so far for each epilogue group
+            int st = 0, st_round = 0;          // the tile's stage and how often the ring wrapped
+            int g = 0;                         // epilogue group of the tile (tiles alternate)
+            int ls0 = 0, lr0 = 0, ls1 = 0, lr1 = 0;   // per group: landing slot, wraps of its ring
             bool ok = true;
             for (int i = 0; i < n_slabs && ok; ++i) {
                 const int qb = i % p.nq;
                 ok = mbar_wait(smem_u32(&q_full[qb]), (i / p.nq) & 1, abort_flag, p.hdr, 4);
                 if (!ok) break;
-                const uint32_t qaddr = smem_u32(q_buf + qb * kQBytes);
-                for (int t = 0; t < n_tiles; ++t, ++it) {
-                    const int g = it & 1;          // epilogue group of tile k = it
-                    const int l = g ? lt1++ : lt0++;
-                    const int st = it % p.stages, slot = g * p.land + l % p.land;
-                    ok = mbar_wait(smem_u32(&k_full[st]), (it / p.stages) & 1, abort_flag, p.hdr, 5);
-                    if (ok && l >= p.land)
-                        ok = mbar_wait(smem_u32(&land_empty[slot]), ((l / p.land) - 1) & 1, abort_flag, p.hdr, 3);
+                // descriptors of the K-major operands advance by constant offsets
+                const uint64_t b0 = smem_desc(smem_u32(q_buf + qb * kQBytes));
+                for (int t = 0; t < n_tiles; ++t) {
+                    const int ls = g ? ls1 : ls0, lr = g ? lr1 : lr0;
+                    const int slot = g * p.land + ls;
+                    ok = mbar_wait(smem_u32(&k_full[st]), st_round & 1, abort_flag, p.hdr, 5);
+                    if (ok && lr > 0) ok = mbar_wait(smem_u32(&land_empty[slot]), (lr - 1) & 1, abort_flag, p.hdr, 3);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kaddr = smem_u32(k_stage + (size_t)st * kStageBytes);
+                    const uint64_t a0 = smem_desc(smem_u32(k_stage + (size_t)st * kStageBytes));
                     const uint32_t d_tmem = tmem_base + (uint32_t)(slot * kRP);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int hf = kk >> 2, ko = kk & 3;
-                        const uint64_t a = smem_desc(kaddr + hf * (kTileRows * 128) + ko * 32);
-                        const uint64_t b = smem_desc(qaddr + hf * (kRP * 128) + ko * 32);
-                        tc_mma(d_tmem, a, b, kIdesc, kk > 0 ? 1u : 0u);
+                        tc_mma(d_tmem, a0 + (uint64_t)((hf * (kTileRows * 128) + ko * 32) >> 4),
+                               b0 + (uint64_t)((hf * (kRP * 128) + ko * 32) >> 4), kIdesc, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&k_empty[st]));
                     tc_commit(smem_u32(&land_full[slot]));
+                    if (++st == p.stages) {
+                        st = 0;
+                        ++st_round;
+                    }
+                    const int ls_n = ls + 1 == p.land ? 0 : ls + 1, lr_n = ls + 1 == p.land ? lr + 1 : lr;
+                    if (g) { ls1 = ls_n; lr1 = lr_n; } else { ls0 = ls_n; lr0 = lr_n; }
+                    g ^= 1;
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&q_empty[qb]));
@@ -1219,7 +1251,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int D, int G>
-sp_status launch_kernel(const CUtensorMap& map, const TcParams& p, cudaStream_t st) {
+sp_status launch_kernel(const KMaps& maps, const TcParams& p, cudaStream_t st) {
     auto kern = tc_score_kernel<D, G>;
     SP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes));
     int per_sm = 0;
@@ -1238,7 +1270,7 @@ sp_status launch_kernel(const CUtensorMap& map, const TcParams& p, cudaStream_t 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, p);
     count_launch();
     if (e != cudaSuccess) {
         set_error("sp_score: cooperative launch of %d CTAs failed: %s", p.P, cudaGetErrorString(e));
@@ -1261,7 +1293,7 @@ size_t score_tc_ws_bytes(const ScoreProblem& q) {
 }
 
 // One prompt (b) of a packed batch: its plan, workspace pointers and launches.
-static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const CUtensorMap& map, int sms,
+static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const KMaps& maps, int sms,
                                void* ws, cudaStream_t st) {
     const int64_t M = q.cu_M_host[b + 1] - q.cu_M_host[b];
     Plan plan;
@@ -1289,14 +1321,14 @@ static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const C
                                         p.lse, p.partials, p.hdr);
     SP_LAUNCH_CHECK();
     switch (q.d * 16 + p.G) {
-        case 64 * 16 + 1: return launch_kernel<64, 1>(map, p, st);
-        case 64 * 16 + 2: return launch_kernel<64, 2>(map, p, st);
-        case 64 * 16 + 4: return launch_kernel<64, 4>(map, p, st);
-        case 64 * 16 + 8: return launch_kernel<64, 8>(map, p, st);
-        case 128 * 16 + 1: return launch_kernel<128, 1>(map, p, st);
-        case 128 * 16 + 2: return launch_kernel<128, 2>(map, p, st);
-        case 128 * 16 + 4: return launch_kernel<128, 4>(map, p, st);
-        case 128 * 16 + 8: return launch_kernel<128, 8>(map, p, st);
+        case 64 * 16 + 1: return launch_kernel<64, 1>(maps, p, st);
+        case 64 * 16 + 2: return launch_kernel<64, 2>(maps, p, st);
+        case 64 * 16 + 4: return launch_kernel<64, 4>(maps, p, st);
+        case 64 * 16 + 8: return launch_kernel<64, 8>(maps, p, st);
+        case 128 * 16 + 1: return launch_kernel<128, 1>(maps, p, st);
+        case 128 * 16 + 2: return launch_kernel<128, 2>(maps, p, st);
+        case 128 * 16 + 4: return launch_kernel<128, 4>(maps, p, st);
+        case 128 * 16 + 8: return launch_kernel<128, 8>(maps, p, st);
         default: break;
     }
     set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, p.G);
@@ -1316,18 +1348,21 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     }
     const int S = q.L * q.H_kv;
     // K viewed as a 2D tensor of L*H_kv*T rows (T: the packed tokens) by d bf16 columns;
-    // 32-row x 64-column boxes.
-    CUtensorMap map;
+    // 64-column boxes of 128 rows (full tiles) and of 32 rows (ragged last tiles).
+    KMaps maps;
     const cuuint64_t gdim[2] = {(cuuint64_t)q.d, (cuuint64_t)S * (cuuint64_t)q.T};
     const cuuint64_t gstride[1] = {(cuuint64_t)q.d * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)kBoxRows};
     const cuuint32_t estride[2] = {1u, 1u};
-    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q.K), gdim, gstride, box,
-                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) {
-        set_error("sp_score: cuTensorMapEncodeTiled failed (%d)", (int)cr);
-        return SP_ECUDA;
+    for (int k = 0; k < 2; ++k) {
+        const cuuint32_t box[2] = {64u, (cuuint32_t)(k == 0 ? kTileRows : kBoxRows)};
+        const CUresult cr = enc(k == 0 ? &maps.full : &maps.tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                const_cast<void*>(q.K), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) {
+            set_error("sp_score: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+            return SP_ECUDA;
+        }
     }
 
     // one prompt after another, each with its own plan; they share the workspace
@@ -1335,7 +1370,7 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
     bool first = true;
     for (int b = 0; b < q.B; ++b) {
         if (q.cu_M_host[b + 1] == q.cu_M_host[b]) continue;
-        const sp_status s = launch_prompt(q, b, first, map, sms, ws, st);
+        const sp_status s = launch_prompt(q, b, first, maps, sms, ws, st);
         if (s != SP_OK) return s;
         first = false;
     }
