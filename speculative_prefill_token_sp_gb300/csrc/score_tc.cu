@@ -46,13 +46,19 @@
 //  * warp 23 (fetch): waits until a slab's lse entries are all tagged and copies
 //    them into a shared-memory ring for the epilogue.
 //
+// Units: every logit, statistic, lse and running max inside this kernel is in
+// base 2 (the natural-log value times log2 e), so each weight is one exp2; the
+// given lse of the lse-in variant is converted on entry and importance is
+// written as exp2 of the running maxima.
+//
 // Precision: P1 statistics use the fp32 logits.  P2 reads w = s - c in fp16,
 // c = the largest logit of the row seen so far in the slab by the warp (taken
-// again whenever a value exceeds it by more than kRefMargin = 2), so w <= 2
-// and its rounding error is at most |w| * 2^-11 (fp16 unit roundoff).  A
-// weight exp(w + c - lse) is then off by at most |w| * 2^-11 relative: < 1e-3
-// for 0 < w <= 2, < 1% for -20 < w <= 0, and for w <= 0 by < 1.8e-4 absolute
-// (c <= lse, and exp(w) * |w| * 2^-11 peaks at w = -1).
+// again whenever a value exceeds it by more than kRefMargin), so w <= 2.08 in
+// natural-log units, and its rounding error is at most |w| * 2^-11 (fp16 unit
+// roundoff; the same bound in either base).  A weight exp(w + c - lse) is then
+// off by at most |w| * 2^-11 relative: < 1.1e-3 for 0 < w <= 2.08, < 1% for
+// -20 < w <= 0, and for w <= 0 by < 1.8e-4 absolute (c <= lse, and
+// exp(w) * |w| * 2^-11 peaks at w = -1).
 //
 // Every wait is bounded: on timeout the kernel records SP_ETIMEOUT in the
 // workspace header, all roles stop, in-flight copies and MMAs are waited for
@@ -80,10 +86,10 @@ constexpr int kUnit = 32;            // token-range granularity
 constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 8;         // tiles per CTA per slab
-// How far (natural-log units) a logit may rise above its row's reference
-// before the epilogue retakes the reference: fp16 offsets below 2 keep the
-// dominant values of a row to 2^-11 relative.
-constexpr float kRefMargin = 2.0f;
+// How far (base-2 units) a logit may rise above its row's reference before the
+// epilogue retakes the reference (3 = 2.08 in natural-log units): fp16 offsets
+// below it keep the dominant values of a row to about 2^-11 relative.
+constexpr float kRefMargin = 3.0f;
 constexpr int kRefBytes = 16 * 16 * 4;  // 16 row references per epilogue warp
 constexpr int kMaxHeld = 12;         // held slabs per epilogue group
 constexpr int kRing = 16;            // entries of the lse ring
@@ -417,7 +423,7 @@ __device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
     if (m2 == -INFINITY) return;
     if (m == -INFINITY) { m = m2; z = z2; return; }
     const float mx = fmaxf(m, m2);
-    z = z * __expf(m - mx) + z2 * __expf(m2 - mx);
+    z = z * ex2_approx(m - mx) + z2 * ex2_approx(m2 - mx);
     m = mx;
 }
 
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
         if (threadIdx.x < kRP) {
             const int r = threadIdx.x;
             float v = 0.f;
-            if (r < p.R) v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N + r / p.G];
+            if (r < p.R) v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N + r / p.G] * 1.4426950408889634f;
             lse[(size_t)s * kRP + r] = (unsigned long long)__float_as_uint(v) | (1ull << 32);
         }
     } else {
@@ -460,6 +466,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
     }
     const int cpr = p.d / 8;                      // 16-byte chunks per row
     uint8_t* img = qimg + (size_t)s * kRP * p.d * 2;
+#pragma unroll 2
     for (int idx = threadIdx.x; idx < kRP * cpr; idx += blockDim.x) {
         const int r = idx / cpr, ch = idx % cpr;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -471,23 +478,54 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
         const size_t off = (size_t)half * (kRP * 128) + (size_t)r * 128 + (size_t)((c ^ (r & 7)) * 16);
         *reinterpret_cast<uint4*>(img + off) = v;
     }
-    // row r (query j = r / G, head g*G + r % G) against look-ahead keys k <= j:
-    // one warp per row, lanes split the dot product
-    for (int r = warp; r < kRP && !p.lse_mode; r += blockDim.x / 32) {
-        float m = -INFINITY, z = 0.f;
-        if (r < p.R) {
-            const int j = r / p.G, h = g * p.G + r % p.G;
-            const __nv_bfloat16* q = Q + (((size_t)j * p.L + l) * p.H + h) * p.d;
-            for (int k = 0; k <= j - p.la_shift; ++k) {
-                const __nv_bfloat16* kk = Kla + (((size_t)l * p.H_kv + g) * (p.N - p.la_shift) + k) * p.d;
-                float u = 0.f;
-                for (int t = lane; t < p.d; t += 32) u = fmaf(__bfloat162float(q[t]), __bfloat162float(kk[t]), u);
+    // row r (query j = r / G, head g*G + r % G) against look-ahead keys k <= j - shift:
+    // eight consecutive lanes per row, one key each (keys k, k + 8, ... folded
+    // in), every dot product from independent 16-byte loads
+    if (!p.lse_mode) {
+        const int nk = p.N - p.la_shift;              // look-ahead keys stored per (layer, KV head)
+        const int sub = lane & 7;
+        for (int r = warp * 4 + (lane >> 3); r < kRP; r += (blockDim.x / 32) * 4) {
+            float m = -INFINITY, z = 0.f;
+            if (r < p.R) {
+                const int j = r / p.G, h = g * p.G + r % p.G;
+                const uint4* q = reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d);
+                for (int k = sub; k <= j - p.la_shift; k += 8) {
+                    const uint4* kk = reinterpret_cast<const uint4*>(Kla + (((size_t)l * p.H_kv + g) * nk + k) * p.d);
+                    // all 16-byte chunks of both rows in flight at once (d <= 128)
+                    uint4 a[16], b[16];
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-                merge(m, z, u * p.scale, 1.f);
+                    for (int c = 0; c < 16; ++c) {
+                        if (c < p.d / 8) {
+                            a[c] = q[c];
+                            b[c] = kk[c];
+                        }
+                    }
+                    float u = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        if (c < p.d / 8) {
+                            const uint32_t aw[4] = {a[c].x, a[c].y, a[c].z, a[c].w};
+                            const uint32_t bw[4] = {b[c].x, b[c].y, b[c].z, b[c].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+                                const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+                                u = fmaf(fa.x, fb.x, u);
+                                u = fmaf(fa.y, fb.y, u);
+                            }
+                        }
+                    }
+                    merge(m, z, u * p.scale_log2e, 1.f);
+                }
             }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+                merge(m, z, m2, z2);
+            }
+            if (sub == 0) la[(size_t)s * kRP + r] = make_float2(m, z);
         }
-        if (lane == 0) la[(size_t)s * kRP + r] = make_float2(m, z);
     }
 }
 
@@ -752,9 +790,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     for (int jl = 0; jl < 16 / G; ++jl) {
                         const int jj = rh * (16 / G) + jl;
                         if (jj < p.N) {
-                            float m = fmaf(x[jl * G], p.scale, -lr[jl * G]);
+                            float m = fmaf(x[jl * G], p.scale_log2e, -lr[jl * G]);
 #pragma unroll
-                            for (int hh = 1; hh < G; ++hh) m = fmaxf(m, fmaf(x[jl * G + hh], p.scale, -lr[jl * G + hh]));
+                            for (int hh = 1; hh < G; ++hh)
+                                m = fmaxf(m, fmaf(x[jl * G + hh], p.scale_log2e, -lr[jl * G + hh]));
                             a[jj * kTileRows] = fmaxf(a[jj * kTileRows], m);
                         }
                     }
@@ -807,9 +846,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));    // this part is read
                     const bool valid = t * kTileRows + tok < len;
+                    const bool full_tile = (t + 1) * kTileRows <= len;
                     float o[16];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) o[r] = fmaf(x[r], p.scale, -ref[r]);
+                    for (int r = 0; r < 16; ++r) o[r] = fmaf(x[r], p.scale_log2e, -ref[r]);
                     bool redo;
                     if (have_ref) {
                         float om[4] = {o[0], o[1], o[2], o[3]};
@@ -824,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                         const float mx = warp_rows16<true>(o, valid);   // finite: a lane is valid
                         const float dm = have_ref ? fmaxf(mx, 0.f) : mx;
                         ref_lane += dm;
-                        z_lane = have_ref ? z_lane * ex2_approx(-dm * 1.4426950408889634f) : 0.f;
+                        z_lane = have_ref ? z_lane * ex2_approx(-dm) : 0.f;
 #pragma unroll
                         for (int r = 0; r < 16; ++r) o[r] -= __shfl_sync(0xffffffffu, dm, 2 * r);
                         if ((lane & 1) == 0) wref[lane >> 1] = ref_lane;
@@ -834,8 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     if (have_ref) {
                         float e[16];
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) e[r] = ex2_approx(o[r] * 1.4426950408889634f);
-                        z_lane += warp_rows16<false>(e, valid);
+                        for (int r = 0; r < 16; ++r) e[r] = ex2_approx(o[r]);
+                        // (the lanes past the range occur only in a ragged last tile)
+                        z_lane += full_tile ? warp_rows16<false>(e, true) : warp_rows16<false>(e, valid);
                     }
                     uint32_t pk[8];
 #pragma unroll
@@ -921,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     if (k < len) {
                         const float* a = acc + (size_t)t * p.N * kTileRows + tok;
                         float sum = 0.f;
-                        for (int jj = 0; jj < p.N; ++jj) sum += expf(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows]));
+                        for (int jj = 0; jj < p.N; ++jj) sum += exp2f(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows]));
                         p.importance[t_begin + k] = sum * inv_n;
                     }
                 }
@@ -952,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                     if (k < len) {
                         float sum = 0.f;
                         for (int jj = 0; jj < p.N; ++jj)
-                            sum += expf(order_decode(__ldcg(&p.acc_glob[(size_t)jj * p.T + t_begin + k])));
+                            sum += exp2f(order_decode(__ldcg(&p.acc_glob[(size_t)jj * p.T + t_begin + k])));
                         p.importance[t_begin + k] = sum * inv_n;
                     }
                 }
@@ -1035,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
                 for (int k = 0; k < 16; ++k) {
                     if (base + 4 * k >= p.Pc) continue;
                     const float2 f = unpack2(v[k]);
-                    zb += f.y * __expf(f.x - mb);
+                    zb += f.y * ex2_approx(f.x - mb);
                 }
                 merge(m, z, mb, zb);
             }
@@ -1051,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             }
             if (part == 0) {
                 merge(m, z, la.x, la.y);
-                const float lse = m + __logf(z);
+                const float lse = m + __log2f(z);     // base 2, like every statistic here
                 st64(&p.lse[(size_t)s * kRP + r], (unsigned long long)__float_as_uint(lse) | (1ull << 32));
             }
             merge_sync();
