@@ -29,6 +29,7 @@ namespace {
 
 constexpr int kMaxBatch = 256;
 constexpr int kSelThreads = 1024;
+constexpr int kRegKeys = 4;             // keys per thread of the in-register top-K (prompts <= 4096 chunks)
 constexpr int kMassMaxChunks = 16384;
 constexpr int kMaxMinTok = 4096;        // keep-rule minimum, at most
 constexpr int kMaxExtras = kMaxMinTok + 6;
@@ -120,26 +121,41 @@ __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, cons
         const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
         const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
         const float2 mmb = g.has_boost && g.normalize ? mm[b] : make_float2(0.f, 0.f);
+        // left to right from 0.0; sixteen loads in flight ahead of the additions
         double s = 0.0;
-        for (int64_t i = lo; i < hi; ++i) s = __dadd_rn(s, token_score(g, imp[m0 + i], i, Mb, mmb));
+        int64_t i = lo;
+        for (; i + 16 <= hi; i += 16) {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = imp[m0 + i + k];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) s = __dadd_rn(s, token_score(g, v[k], i + k, Mb, mmb));
+        }
+        for (; i < hi; ++i) s = __dadd_rn(s, token_score(g, imp[m0 + i], i, Mb, mmb));
         sums[gc] = s;
         means[gc] = __ddiv_rn(s, (double)(hi - lo));
     }
 }
 
-// (2) centred average pool over the prompt's own chunks; edges average in-range chunks.
+// (2) centred average pool over the prompt's own chunks; edges average in-range
+// chunks (left to right from 0.0, one divide by the window's count).
+__device__ __forceinline__ double pooled_at(const SelGeo& g, const double* __restrict__ means, int64_t c0, int64_t nc,
+                                            int64_t c) {
+    const int r = (g.pool_k - 1) / 2;
+    const int64_t lo = c - r < 0 ? 0 : c - r;
+    const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
+    double s = 0.0;
+    for (int64_t t = lo; t <= hi; ++t) s = __dadd_rn(s, means[c0 + t]);
+    return __ddiv_rn(s, (double)(hi - lo + 1));
+}
+
 __global__ void pool_kernel(const SelGeo g, const double* __restrict__ means, double* __restrict__ pooled) {
     const int64_t total = g.cn[g.B];
-    const int r = (g.pool_k - 1) / 2;
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
          gc += (int64_t)gridDim.x * blockDim.x) {
         const int b = find_batch(g.cn, g.B, gc);
-        const int64_t c0 = g.cn[b], nc = g.cn[b + 1] - c0, c = gc - c0;
-        const int64_t lo = c - r < 0 ? 0 : c - r;
-        const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
-        double s = 0.0;
-        for (int64_t t = lo; t <= hi; ++t) s = __dadd_rn(s, means[c0 + t]);
-        pooled[gc] = __ddiv_rn(s, (double)(hi - lo + 1));
+        const int64_t c0 = g.cn[b], nc = g.cn[b + 1] - c0;
+        pooled[gc] = pooled_at(g, means, c0, nc, gc - c0);
     }
 }
 
@@ -169,6 +185,97 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
     return base + x - v;
 }
 
+// Top-K of a prompt with at most kSelThreads * kRegKeys chunks: the pooled keys
+// (chunk c = q * blockDim.x + tid in key[q]) stay in registers through a radix
+// select, 8 bits per pass from the most significant, counted with
+// warp-aggregated shared-memory atomics.  The passes stop once every key with
+// the selected prefix is taken.  Then keys above the prefix, and the first
+// `remaining` equal to it in chunk order, are kept.
+__device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double* __restrict__ means, int64_t c0, int nc, int64_t Mb,
+                                  int kc, int* __restrict__ flags, int64_t* __restrict__ offs,
+                                  int64_t* __restrict__ n_kept_b, unsigned* hist, long long* scan_sh,
+                                  uint64_t* s_prefix, int* s_remaining, int* s_done) {
+    const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
+    const int rounds = (nc + bd - 1) / bd;
+    uint64_t key[kRegKeys];
+#pragma unroll
+    for (int q = 0; q < kRegKeys; ++q) {
+        const int c = q * bd + tid;
+        key[q] = c < nc ? order_key(pooled_at(g, means, c0, nc, c)) : 0ull;
+    }
+    uint64_t prefix = 0, pmask = 0;
+    int remaining = kc;
+    for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        for (int i = tid; i < 256; i += bd) hist[i] = 0;
+        if (tid == 0) *s_done = 0;
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kRegKeys; ++q) {
+            const int c = q * bd + tid;
+            const bool take = c < nc && (key[q] & pmask) == prefix;
+            const unsigned digit = take ? (unsigned)((key[q] >> shift) & 255u) : 256u;
+            const unsigned peers = __match_any_sync(0xffffffffu, digit);
+            if (take && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (unsigned)__popc(peers));
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // lane covers digits [8*lane, 8*lane+8); count keys with a larger digit.
+            unsigned local = 0;
+            for (int q = 0; q < 8; ++q) local += hist[tid * 8 + q];
+            unsigned x = local;
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_down_sync(0xffffffffu, x, o);
+                if (tid + o < 32) x += y;
+            }
+            const unsigned above = x - local;
+            if (above < (unsigned)remaining && above + local >= (unsigned)remaining) {
+                unsigned cum = above;
+                for (int q = 7; q >= 0; --q) {
+                    const unsigned hq = hist[tid * 8 + q];
+                    if (cum + hq >= (unsigned)remaining) {
+                        *s_prefix = prefix | ((uint64_t)(tid * 8 + q) << shift);
+                        *s_remaining = remaining - (int)cum;
+                        *s_done = hq == (unsigned)(remaining - (int)cum) ? 1 : 0;
+                        break;
+                    }
+                    cum += hq;
+                }
+            }
+        }
+        __syncthreads();
+        prefix = *s_prefix;
+        remaining = *s_remaining;
+        pmask |= (0xFFull << shift);
+        const bool done = *s_done != 0;
+        __syncthreads();
+        if (done) break;
+    }
+    long long taken_eq = 0, running = 0;
+#pragma unroll
+    for (int q = 0; q < kRegKeys; ++q) {
+        if (q >= rounds) break;
+        const int c = q * bd + tid;
+        const bool in = c < nc;
+        const uint64_t k = key[q] & pmask;
+        const bool gt = in && k > prefix, eq = in && k == prefix;
+        long long tot_eq;
+        const long long rank = block_exclusive_scan(eq ? 1 : 0, scan_sh, &tot_eq);
+        const bool keep = gt || (eq && taken_eq + rank < remaining);
+        const int64_t lo = (int64_t)c * g.chunk;
+        const long long sz = keep ? (long long)(min(lo + (int64_t)g.chunk, Mb) - lo) : 0;
+        long long tot_sz;
+        const long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        if (in) {
+            flags[c0 + c] = keep ? 1 : 0;
+            offs[c0 + c] = running + off;
+        }
+        taken_eq += tot_eq;
+        running += tot_sz;
+    }
+    if (tid == 0) *n_kept_b = running;
+}
+
 // (3) per-prompt selection.  Writes keep flags, kept-size offsets and n_kept.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, const double* __restrict__ sums,
                                                              const double* __restrict__ means,
@@ -182,6 +289,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
     __shared__ uint64_t s_prefix;
     __shared__ int s_remaining;
     __shared__ int s_kstar;
+    __shared__ int s_done;
 
     const int b = blockIdx.x;
     const int64_t c0 = g.cn[b];
@@ -198,6 +306,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         const float prod = (float)nc * (float)g.rate;
         int kc = (int)ceilf(prod);
         kc = kc < 1 ? 1 : (kc > nc ? nc : kc);
+        if (nc <= (int)blockDim.x * kRegKeys) {
+            topk_in_registers(g, means, c0, nc, Mb, kc, flags, offs, n_kept + b, hist, scan_sh, &s_prefix,
+                              &s_remaining, &s_done);
+            return;
+        }
         // Radix select (8 bits per pass, most significant first) of the kc-th
         // largest key; afterwards `remaining` keys equal to it must be taken.
         uint64_t prefix = 0, pmask = 0;
@@ -495,11 +608,12 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
         SP_LAUNCH_CHECK();
     }
     if (total > 0) {
-        const int blocks = (int)std::min<int64_t>((total + 255) / 256, 2048);
-        chunk_kernel<<<blocks, 256, 0, st>>>(g, p.importance, mm, sums, means);
+        // small blocks: the fixed-order fp64 sums run on as many SMs as possible
+        const int blocks = (int)std::min<int64_t>((total + 63) / 64, 8192);
+        chunk_kernel<<<blocks, 64, 0, st>>>(g, p.importance, mm, sums, means);
         SP_LAUNCH_CHECK();
-        if (p.mode == SP_SELECT_TOPK) {
-            pool_kernel<<<blocks, 256, 0, st>>>(g, means, pooled);
+        if (p.mode == SP_SELECT_TOPK && p.max_nc > (int64_t)kSelThreads * kRegKeys) {
+            pool_kernel<<<(int)std::min<int64_t>((total + 255) / 256, 2048), 256, 0, st>>>(g, means, pooled);
             SP_LAUNCH_CHECK();
         }
     }
