@@ -30,6 +30,7 @@ namespace {
 constexpr int kMaxBatch = 256;
 constexpr int kSelThreads = 1024;
 constexpr int kRegKeys = 4;             // keys per thread of the in-register top-K (prompts <= 4096 chunks)
+constexpr int kInlinePosChunk = 256;    // chunks up to this size get their positions from the selection kernel
 constexpr int kMassMaxChunks = 16384;
 constexpr int kMaxMinTok = 4096;        // keep-rule minimum, at most
 constexpr int kMaxExtras = kMaxMinTok + 6;
@@ -112,7 +113,9 @@ __device__ __forceinline__ double token_score(const SelGeo& g, float v, int64_t 
 
 // (1) chunk sums (left to right from 0.0) and means (one divide).
 __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const float2* __restrict__ mm,
-                             double* __restrict__ sums, double* __restrict__ means) {
+                             double* __restrict__ sums, double* __restrict__ means, int32_t* __restrict__ hdr) {
+    // a fresh status for the call (the workspace header)
+    if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
     const int64_t total = g.cn[g.B];
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
          gc += (int64_t)gridDim.x * blockDim.x) {
@@ -193,8 +196,8 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 // `remaining` equal to it in chunk order, are kept.
 __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double* __restrict__ means, int64_t c0, int nc, int64_t Mb,
                                   int kc, int* __restrict__ flags, int64_t* __restrict__ offs,
-                                  int64_t* __restrict__ n_kept_b, unsigned* hist, long long* scan_sh,
-                                  uint64_t* s_prefix, int* s_remaining, int* s_done) {
+                                  int32_t* __restrict__ kept_b, int64_t* __restrict__ n_kept_b, unsigned* hist,
+                                  long long* scan_sh, uint64_t* s_prefix, int* s_remaining, int* s_done) {
     const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
     const int rounds = (nc + bd - 1) / bd;
     uint64_t key[kRegKeys];
@@ -269,6 +272,8 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
         if (in) {
             flags[c0 + c] = keep ? 1 : 0;
             offs[c0 + c] = running + off;
+            if (keep && g.chunk <= kInlinePosChunk)
+                for (long long t = 0; t < sz; ++t) kept_b[running + off + t] = (int32_t)(lo + t);
         }
         taken_eq += tot_eq;
         running += tot_sz;
@@ -282,6 +287,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
                                                              const double* __restrict__ pooled,
                                                              int* __restrict__ flags,
                                                              int64_t* __restrict__ offs,
+                                                             int32_t* __restrict__ kept_pos,
                                                              int64_t* __restrict__ n_kept) {
     extern __shared__ __align__(16) unsigned char dsm[];
     __shared__ long long scan_sh[32];
@@ -307,8 +313,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         int kc = (int)ceilf(prod);
         kc = kc < 1 ? 1 : (kc > nc ? nc : kc);
         if (nc <= (int)blockDim.x * kRegKeys) {
-            topk_in_registers(g, means, c0, nc, Mb, kc, flags, offs, n_kept + b, hist, scan_sh, &s_prefix,
-                              &s_remaining, &s_done);
+            topk_in_registers(g, means, c0, nc, Mb, kc, flags, offs, kept_pos + g.cu[b], n_kept + b, hist, scan_sh,
+                              &s_prefix, &s_remaining, &s_done);
             return;
         }
         // Radix select (8 bits per pass, most significant first) of the kc-th
@@ -432,6 +438,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         long long tot_sz;
         long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
         if (in) offs[c0 + c] = running + off;
+        if (keep && g.chunk <= kInlinePosChunk)
+            for (long long t = 0; t < sz; ++t) kept_pos[g.cu[b] + running + off + t] = (int32_t)(lo + t);
         running += tot_sz;
     }
     if (tid == 0) n_kept[b] = running;
@@ -601,8 +609,9 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     int* flags = reinterpret_cast<int*>(w + lo.flags);
     int64_t* offs = reinterpret_cast<int64_t*>(w + lo.offs);
 
-    SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
     const int64_t total = g.cn[p.B];
+    // the header is cleared by the chunk kernel (or here, when there are no chunks)
+    if (total == 0 || (p.has_boost && p.boost.normalize)) SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
     if (p.has_boost && p.boost.normalize) {
         minmax_kernel<<<p.B, 1024, 0, st>>>(g, p.importance, mm);
         SP_LAUNCH_CHECK();
@@ -610,7 +619,8 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     if (total > 0) {
         // small blocks: the fixed-order fp64 sums run on as many SMs as possible
         const int blocks = (int)std::min<int64_t>((total + 63) / 64, 8192);
-        chunk_kernel<<<blocks, 64, 0, st>>>(g, p.importance, mm, sums, means);
+        int32_t* hdr = (p.has_boost && p.boost.normalize) ? nullptr : static_cast<int32_t*>(ws);
+        chunk_kernel<<<blocks, 64, 0, st>>>(g, p.importance, mm, sums, means, hdr);
         SP_LAUNCH_CHECK();
         if (p.mode == SP_SELECT_TOPK && p.max_nc > (int64_t)kSelThreads * kRegKeys) {
             pool_kernel<<<(int)std::min<int64_t>((total + 255) / 256, 2048), 256, 0, st>>>(g, means, pooled);
@@ -625,9 +635,13 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     }
     SP_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)std::max<size_t>(dyn, 0)));
-    select_kernel<<<p.B, kSelThreads, dyn, st>>>(g, sums, means, pooled, flags, offs, p.n_kept);
+    select_kernel<<<p.B, kSelThreads, dyn, st>>>(g, sums, means, pooled, flags, offs, p.kept_pos, p.n_kept);
     SP_LAUNCH_CHECK();
-    if (p.T > 0) {
+    // positions not written by the selection kernel: chunks above kInlinePosChunk
+    // tokens, or top-K prompts too long for the in-register path
+    const bool inline_pos = p.chunk <= kInlinePosChunk &&
+                            (p.mode == SP_SELECT_MASS || p.max_nc <= (int64_t)kSelThreads * kRegKeys);
+    if (p.T > 0 && !inline_pos) {
         const int blocks = (int)std::min<int64_t>((p.T + 255) / 256, 4096);
         compact_kernel<<<blocks, 256, 0, st>>>(g, flags, offs, p.kept_pos);
         SP_LAUNCH_CHECK();
