@@ -67,6 +67,9 @@
 
 #include <cuda.h>
 #include <cuda_fp16.h>
+
+#include <algorithm>
+#include <vector>
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -136,6 +139,17 @@ struct TcParams {
     float* importance;
     unsigned* acc_glob;             // [N][T] order-preserving codes of the combined maxima (F > 1)
     int* arrivals;                  // [Pc] CTAs of a range done with their maxima (F > 1)
+    const __nv_bfloat16* Qp;        // the prompt's look-ahead queries [N, L, H, d] (preparation)
+    const __nv_bfloat16* Klap;      // its look-ahead keys [L, H_kv, N - la_shift, d] (preparation)
+};
+
+// Prompts of one batched launch ("wave"): prompt b owns CTAs [cta0[b], cta0[b+1])
+// and has its own plan and workspace slice.
+constexpr int kMaxWave = 32;
+struct TcBatch {
+    int nb;
+    int cta0[kMaxWave + 1];
+    TcParams p[kMaxWave];
 };
 
 // ---------------------------------------------------------------------------
@@ -434,12 +448,15 @@ __device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
 // also clears the status.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __nv_bfloat16* __restrict__ Q,
-                                                      const __nv_bfloat16* __restrict__ Kla,
-                                                      uint8_t* __restrict__ qimg, float2* __restrict__ la,
-                                                      unsigned long long* __restrict__ lse,
-                                                      unsigned long long* __restrict__ partials, WsHeader* hdr) {
-    const int s = blockIdx.x;
+// Block s (one per slab) of one prompt's preparation.
+__device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
+    const __nv_bfloat16* __restrict__ Q = p.Qp;
+    const __nv_bfloat16* __restrict__ Kla = p.Klap;
+    uint8_t* __restrict__ qimg = const_cast<uint8_t*>(p.qimg);
+    float2* __restrict__ la = const_cast<float2*>(p.la);
+    unsigned long long* __restrict__ lse = p.lse;
+    unsigned long long* __restrict__ partials = p.partials;
+    WsHeader* hdr = p.hdr;
     const int l = s / p.H_kv, g = s % p.H_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (p.first && s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
@@ -460,9 +477,9 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
         // combined running maxima (0 is below every encoded float) and the
         // per-range arrival counters
         const size_t n = (size_t)p.N * p.T;
-        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        for (size_t i = (size_t)s * blockDim.x + threadIdx.x; i < n; i += (size_t)p.S * blockDim.x)
             p.acc_glob[i] = 0u;
-        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.Pc; i += gridDim.x * blockDim.x) p.arrivals[i] = 0;
+        for (int i = s * blockDim.x + threadIdx.x; i < p.Pc; i += p.S * blockDim.x) p.arrivals[i] = 0;
     }
     const int cpr = p.d / 8;                      // 16-byte chunks per row
     uint8_t* img = qimg + (size_t)s * kRP * p.d * 2;
@@ -529,6 +546,16 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcParams p, const __
     }
 }
 
+__global__ void __launch_bounds__(256) tc_prep_kernel(const __grid_constant__ TcParams p) {
+    tc_prep_body(p, blockIdx.x);
+}
+
+// All prompts of a wave: blocks b * S .. b * S + S - 1 prepare prompt b.
+__global__ void __launch_bounds__(256) tc_prep_batch_kernel(const __grid_constant__ TcBatch bt) {
+    const int S = bt.p[0].S;
+    tc_prep_body(bt.p[blockIdx.x / S], blockIdx.x % S);
+}
+
 // ---------------------------------------------------------------------------
 // The persistent scoring kernel
 // ---------------------------------------------------------------------------
@@ -551,8 +578,7 @@ struct KMaps {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ KMaps kmaps,
-                                                                const TcParams p) {
+__device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams& p, const int c) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int kHalves = D / 64;
@@ -561,7 +587,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     constexpr uint32_t kIdesc = instr_desc_bf16(kRP);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x;
     // Slab class and token range of this CTA: it takes slabs s = cf, cf + F, ...
     // (n_slabs of them) over the tokens [t_begin, t_end) of each.  The F CTAs
     // with the same range combine their running maxima at the end.
@@ -1139,6 +1164,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     }
 }
 
+// One prompt: CTA c of p.P.
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ KMaps kmaps,
+                                                                const __grid_constant__ TcParams p) {
+    tc_score_body<D, G>(kmaps, p, blockIdx.x);
+}
+
+// A wave of prompts: CTA blockIdx.x works for the prompt whose range holds it.
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) tc_score_batch_kernel(const __grid_constant__ KMaps kmaps,
+                                                                      const __grid_constant__ TcBatch bt) {
+    int b = 0;
+    while (b + 1 < bt.nb && (int)blockIdx.x >= bt.cta0[b + 1]) ++b;
+    tc_score_body<D, G>(kmaps, bt.p[b], (int)blockIdx.x - bt.cta0[b]);
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1291,34 +1332,127 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int D, int G>
-sp_status launch_kernel(const KMaps& maps, const TcParams& p, cudaStream_t st) {
-    auto kern = tc_score_kernel<D, G>;
-    SP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes));
+// Cooperative launch of `grid` CTAs of `kern` (one prompt or a wave).
+template <typename Kern, typename Arg>
+sp_status launch_coop(Kern kern, const KMaps& maps, const Arg& arg, int grid, int smem_bytes, cudaStream_t st) {
+    SP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes));
     int per_sm = 0;
-    SP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, p.smem_bytes));
+    SP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes));
     if (per_sm < 1) {
-        set_error("sp_score: the tensor-core kernel does not fit on an SM (%d bytes of shared memory)", p.smem_bytes);
+        set_error("sp_score: the tensor-core kernel does not fit on an SM (%d bytes of shared memory)", smem_bytes);
         return SP_EUNSUPPORTED;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.P);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, arg);
     count_launch();
     if (e != cudaSuccess) {
-        set_error("sp_score: cooperative launch of %d CTAs failed: %s", p.P, cudaGetErrorString(e));
+        set_error("sp_score: cooperative launch of %d CTAs failed: %s", grid, cudaGetErrorString(e));
         return SP_ECUDA;
     }
     return SP_OK;
 }
+
+template <int D, int G>
+sp_status launch_kernel(const KMaps& maps, const TcParams& p, cudaStream_t st) {
+    return launch_coop(tc_score_kernel<D, G>, maps, p, p.P, p.smem_bytes, st);
+}
+
+template <int D, int G>
+sp_status launch_batch(const KMaps& maps, const TcBatch& bt, int smem_bytes, cudaStream_t st) {
+    return launch_coop(tc_score_batch_kernel<D, G>, maps, bt, bt.cta0[bt.nb], smem_bytes, st);
+}
+
+// The prompt's pointers: its workspace slice starts at w; the status header is
+// always the first 256 bytes of the whole workspace.
+void bind_prompt(const ScoreProblem& q, int b, bool first, uint8_t* ws, uint8_t* w, Plan& plan) {
+    TcParams& p = plan.p;
+    p.tok0 = q.cu_M_host[b];
+    p.first = first ? 1 : 0;
+    p.hdr = reinterpret_cast<WsHeader*>(ws);
+    p.qimg = w + plan.off_qimg;
+    p.la = reinterpret_cast<const float2*>(w + plan.off_la);
+    p.partials = reinterpret_cast<unsigned long long*>(w + plan.off_partials);
+    p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
+    p.importance = q.importance + q.cu_M_host[b];
+    p.acc_glob = reinterpret_cast<unsigned*>(w + plan.off_acc_glob);
+    p.arrivals = reinterpret_cast<int*>(w + plan.off_arrivals);
+    p.Qp = static_cast<const __nv_bfloat16*>(q.Q) + (size_t)b * q.N * q.L * q.H * q.d;
+    p.Klap = q.Kla ? static_cast<const __nv_bfloat16*>(q.Kla) + (size_t)b * q.L * q.H_kv * (q.N - q.la_shift) * q.d
+                   : nullptr;
+}
+
+// Waves of a batch: consecutive non-empty prompts, at most kMaxWave of them,
+// whose minimum CTA counts (kMaxTiles tiles per CTA and slab) fit on the SMs
+// together.  Each prompt gets its minimum plus a share of the spare CTAs in
+// proportion to its length, its own plan and its own workspace slice.
+struct Wave {
+    std::vector<int> prompts;
+    std::vector<Plan> plans;
+    std::vector<size_t> offs;   // workspace slice of each prompt
+    size_t bytes = 0;           // the wave's workspace
+    int smem = 0;               // the largest plan's shared memory
+};
+
+bool plan_waves(const ScoreProblem& q, int sms, std::vector<Wave>& waves) {
+    waves.clear();
+    const int64_t per_cta = (int64_t)kMaxTiles * kTileRows;      // tokens of a slab one CTA can take
+    auto len = [&](int b) { return q.cu_M_host[b + 1] - q.cu_M_host[b]; };
+    auto min_ctas = [&](int b) { return (int)((len(b) + per_cta - 1) / per_cta); };
+    std::vector<int> cur;
+    int64_t tot = 0;
+    int need = 0;
+    auto flush = [&]() -> bool {
+        if (cur.empty()) return true;
+        Wave w;
+        w.prompts = cur;
+        const int n = (int)cur.size();
+        std::vector<int> P(n);
+        const int spare = sms - need;
+        int used = 0;
+        for (int i = 0; i < n; ++i) {
+            P[i] = min_ctas(cur[i]) + (int)((int64_t)spare * len(cur[i]) / tot);
+            used += P[i];
+        }
+        for (int i = 0; used < sms; i = (i + 1) % n, ++used) ++P[i];
+        size_t off = 0;
+        for (int i = 0; i < n; ++i) {
+            Plan plan;
+            if (!make_plan(q, len(cur[i]), P[i], plan)) return false;
+            w.plans.push_back(plan);
+            w.offs.push_back(off);
+            off += align_up(plan.total);
+            w.smem = std::max(w.smem, plan.p.smem_bytes);
+        }
+        w.bytes = off;
+        waves.push_back(std::move(w));
+        cur.clear();
+        tot = 0;
+        need = 0;
+        return true;
+    };
+    for (int b = 0; b < q.B; ++b) {
+        if (len(b) == 0) continue;
+        if (min_ctas(b) > sms) return false;
+        if (!cur.empty() && (need + min_ctas(b) > sms || (int)cur.size() == kMaxWave))
+            if (!flush()) return false;
+        cur.push_back(b);
+        tot += len(b);
+        need += min_ctas(b);
+    }
+    return flush();
+}
+
+// Batches go in waves when every prompt of every wave has a plan.
+bool use_waves(const ScoreProblem& q) { return q.B > 1; }
 
 }  // namespace
 
@@ -1328,9 +1462,15 @@ bool score_tc_supported(const ScoreProblem& q) {
 }
 
 size_t score_tc_ws_bytes(const ScoreProblem& q) {
-    // the workspace is reused prompt after prompt; the largest prompt needs the most
+    // prompt after prompt, the workspace is reused: the largest prompt needs the most
     Plan plan;
-    return make_plan(q, q.max_M, kMaxCtas, plan) ? plan.total : 0;
+    size_t bytes = make_plan(q, q.max_M, kMaxCtas, plan) ? plan.total : 0;
+    if (bytes > 0 && use_waves(q)) {
+        std::vector<Wave> waves;
+        if (plan_waves(q, sm_count_or(148), waves))
+            for (const Wave& w : waves) bytes = std::max(bytes, w.bytes);
+    }
+    return bytes;
 }
 
 // One prompt (b) of a packed batch: its plan, workspace pointers and launches.
@@ -1342,24 +1482,10 @@ static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const K
         set_error("sp_score: prompt %d (%lld tokens) is outside the tensor-core path", b, (long long)M);
         return SP_EUNSUPPORTED;
     }
-    TcParams& p = plan.p;
-    p.tok0 = q.cu_M_host[b];
-    p.first = first ? 1 : 0;
     uint8_t* w = static_cast<uint8_t*>(ws);
-    p.hdr = reinterpret_cast<WsHeader*>(w);
-    p.qimg = w + plan.off_qimg;
-    p.la = reinterpret_cast<const float2*>(w + plan.off_la);
-    p.partials = reinterpret_cast<unsigned long long*>(w + plan.off_partials);
-    p.lse = reinterpret_cast<unsigned long long*>(w + plan.off_lse);
-    p.importance = q.importance + q.cu_M_host[b];
-    p.acc_glob = reinterpret_cast<unsigned*>(w + plan.off_acc_glob);
-    p.arrivals = reinterpret_cast<int*>(w + plan.off_arrivals);
-    const __nv_bfloat16* Qb = static_cast<const __nv_bfloat16*>(q.Q) + (size_t)b * q.N * q.L * q.H * q.d;
-    const __nv_bfloat16* Klab = q.Kla ? static_cast<const __nv_bfloat16*>(q.Kla) +
-                                            (size_t)b * q.L * q.H_kv * (q.N - q.la_shift) * q.d
-                                      : nullptr;
-    tc_prep_kernel<<<p.S, 256, 0, st>>>(p, Qb, Klab, w + plan.off_qimg, reinterpret_cast<float2*>(w + plan.off_la),
-                                        p.lse, p.partials, p.hdr);
+    bind_prompt(q, b, first, w, w, plan);
+    const TcParams& p = plan.p;
+    tc_prep_kernel<<<p.S, 256, 0, st>>>(p);
     SP_LAUNCH_CHECK();
     switch (q.d * 16 + p.G) {
         case 64 * 16 + 1: return launch_kernel<64, 1>(maps, p, st);
@@ -1373,6 +1499,37 @@ static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const K
         default: break;
     }
     set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, p.G);
+    return SP_EUNSUPPORTED;
+}
+
+// One wave: one preparation launch and one cooperative launch for all its prompts.
+static sp_status launch_wave(const ScoreProblem& q, Wave& wv, bool first, const KMaps& maps, void* ws,
+                             cudaStream_t st) {
+    static_assert(sizeof(TcBatch) < 32000, "a wave's parameters must fit the kernel parameter space");
+    TcBatch bt;
+    bt.nb = (int)wv.prompts.size();
+    bt.cta0[0] = 0;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    for (int i = 0; i < bt.nb; ++i) {
+        Plan& plan = wv.plans[i];
+        bind_prompt(q, wv.prompts[i], first && i == 0, w, w + wv.offs[i], plan);
+        bt.p[i] = plan.p;
+        bt.cta0[i + 1] = bt.cta0[i] + plan.p.P;
+    }
+    tc_prep_batch_kernel<<<bt.nb * bt.p[0].S, 256, 0, st>>>(bt);
+    SP_LAUNCH_CHECK();
+    switch (q.d * 16 + bt.p[0].G) {
+        case 64 * 16 + 1: return launch_batch<64, 1>(maps, bt, wv.smem, st);
+        case 64 * 16 + 2: return launch_batch<64, 2>(maps, bt, wv.smem, st);
+        case 64 * 16 + 4: return launch_batch<64, 4>(maps, bt, wv.smem, st);
+        case 64 * 16 + 8: return launch_batch<64, 8>(maps, bt, wv.smem, st);
+        case 128 * 16 + 1: return launch_batch<128, 1>(maps, bt, wv.smem, st);
+        case 128 * 16 + 2: return launch_batch<128, 2>(maps, bt, wv.smem, st);
+        case 128 * 16 + 4: return launch_batch<128, 4>(maps, bt, wv.smem, st);
+        case 128 * 16 + 8: return launch_batch<128, 8>(maps, bt, wv.smem, st);
+        default: break;
+    }
+    set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, bt.p[0].G);
     return SP_EUNSUPPORTED;
 }
 
@@ -1406,8 +1563,24 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
         }
     }
 
-    // one prompt after another, each with its own plan; they share the workspace
-    // (stream order separates them)
+    // a batch: wave after wave, each wave's prompts side by side on the SMs
+    // (stream order separates the waves, which reuse the workspace)
+    std::vector<Wave> waves;
+    if (use_waves(q) && plan_waves(q, sms, waves)) {
+        size_t need = 0;
+        for (const Wave& w : waves) need = std::max(need, w.bytes);
+        if (need <= score_tc_ws_bytes(q)) {
+            bool first = true;
+            for (Wave& w : waves) {
+                const sp_status s = launch_wave(q, w, first, maps, ws, st);
+                if (s != SP_OK) return s;
+                first = false;
+            }
+            return SP_OK;
+        }
+    }
+    // otherwise one prompt after another, each with its own plan over all SMs;
+    // they share the workspace (stream order separates them)
     bool first = true;
     for (int b = 0; b < q.B; ++b) {
         if (q.cu_M_host[b + 1] == q.cu_M_host[b]) continue;
