@@ -782,7 +782,8 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
         float* wref = rbuf + ew * 16;                  // the warp's 16 row references (P1)
         const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * tpg * 16 + rh * 8);
         const int odd = n_tiles & 1;
-        int lt = 0;                                    // landing tiles consumed so far
+        int ls = 0, lph = 0;                           // next landing tile of the group's ring, its phase
+        int hs1 = 0, hs2 = 0;                          // held slots of the next P1 and P2 slabs
         uint32_t chg = 0;                              // held tiles (hs * tpg + j) whose references P2 reloads
         bool ok = true;
         if (p.lse_mode) {
@@ -798,9 +799,9 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                 for (int r = 0; r < 16; ++r) lr[r] = lse_ring[q * kRP + rh * 16 + r];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&lse_empty[q]));
-                for (int t = t0; t < n_tiles; t += 2, ++lt) {
-                    const int slot = grp * p.land + lt % p.land;
-                    if (!warp_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6)) {
+                for (int t = t0; t < n_tiles; t += 2) {
+                    const int slot = grp * p.land + ls;
+                    if (!warp_wait(smem_u32(&land_full[slot]), lph, abort_flag, p.hdr, 6)) {
                         ok = false;
                         break;
                     }
@@ -810,6 +811,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));
+                    if (++ls == p.land) { ls = 0; lph ^= 1; }
                     float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
 #pragma unroll
                     for (int jl = 0; jl < 16 / G; ++jl) {
@@ -828,7 +830,8 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
         for (int i = 0; i < (p.lse_mode ? 0 : n_slabs + p.lag) && ok; ++i) {
             // ---- P1: statistics of this CTA's i-th slab over the group's tiles, as fp16 offsets ----
             if (i < n_slabs) {
-                const int s = i, q = s % kStatsRing, hs = s % p.held;
+                const int s = i, q = s % kStatsRing, hs = hs1;
+                if (++hs1 == p.held) hs1 = 0;
                 const int t0 = (grp + s * odd) & 1;    // this group's first tile of the slab
                 if (s >= kStatsRing &&
                     !warp_wait(smem_u32(&stats_empty[q]), ((s / kStatsRing) - 1) & 1, abort_flag, p.hdr, 7)) {
@@ -851,8 +854,8 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                 float z_lane = 0.f;                    // and that row's sum of exp(s - ref)
                 bool have_ref = false;
                 chg &= ~(((1u << tpg) - 1u) << (hs * tpg));
-                for (int t = t0, j = 0; t < n_tiles; t += 2, ++j, ++lt) {
-                    const int slot = grp * p.land + lt % p.land;
+                for (int t = t0, j = 0; t < n_tiles; t += 2, ++j) {
+                    const int slot = grp * p.land + ls;
                     float ref[16];                     // read while the landing tile is awaited
                     if (have_ref) {
                         load16(wref, ref);
@@ -860,7 +863,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
 #pragma unroll
                         for (int r = 0; r < 16; ++r) ref[r] = 0.f;
                     }
-                    if (!warp_wait(smem_u32(&land_full[slot]), (lt / p.land) & 1, abort_flag, p.hdr, 6)) {
+                    if (!warp_wait(smem_u32(&land_full[slot]), lph, abort_flag, p.hdr, 6)) {
                         ok = false;
                         break;
                     }
@@ -870,6 +873,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));    // this part is read
+                    if (++ls == p.land) { ls = 0; lph ^= 1; }
                     const bool valid = t * kTileRows + tok < len;
                     const bool full_tile = (t + 1) * kTileRows <= len;
                     float o[16];
@@ -928,7 +932,8 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
             }
             // ---- P2: normalise the group's tiles of the (i - lag)-th slab, fold the max ----
             if (i >= p.lag) {
-                const int s = i - p.lag, q = s % kRing, hs = s % p.held;
+                const int s = i - p.lag, q = s % kRing, hs = hs2;
+                if (++hs2 == p.held) hs2 = 0;
                 const int t0 = (grp + s * odd) & 1;
                 if (!warp_wait(smem_u32(&lse_full[q]), (s / kRing) & 1, abort_flag, p.hdr, 8)) {
                     ok = false;
