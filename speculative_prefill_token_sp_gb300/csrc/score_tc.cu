@@ -560,15 +560,13 @@ __global__ void __launch_bounds__(256) tc_prep_batch_kernel(const __grid_constan
 // The persistent scoring kernel
 // ---------------------------------------------------------------------------
 
-// Lane 0 of the warp waits for the barrier phase; the outcome is shared with
-// the whole warp, which then leaves or goes on together.
+// Every lane of the warp tests the barrier phase (no divergent branch on the
+// common path); a vote makes the outcome the warp's, which then leaves or goes
+// on together.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
                                           int where) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, hdr, where) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    const bool ok = mbar_wait(bar, parity, abort_flag, hdr, where);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // K viewed as a 2D tensor of rows by d bf16 columns, in 64-column boxes of 128
