@@ -508,27 +508,31 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
                 const uint4* q = reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d);
                 for (int k = sub; k <= j - p.la_shift; k += 8) {
                     const uint4* kk = reinterpret_cast<const uint4*>(Kla + (((size_t)l * p.H_kv + g) * nk + k) * p.d);
-                    // all 16-byte chunks of both rows in flight at once (d <= 128)
-                    uint4 a[16], b[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        if (c < p.d / 8) {
-                            a[c] = q[c];
-                            b[c] = kk[c];
-                        }
-                    }
+                    // eight 16-byte chunks of both rows in flight at a time (d <= 128)
                     float u = 0.f;
+                    for (int c0 = 0; c0 < p.d / 8; c0 += 8) {
+                        uint4 a[8], b[8];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        if (c < p.d / 8) {
-                            const uint32_t aw[4] = {a[c].x, a[c].y, a[c].z, a[c].w};
-                            const uint32_t bw[4] = {b[c].x, b[c].y, b[c].z, b[c].w};
+                        for (int c = 0; c < 8; ++c) {
+                            if (c0 + c < p.d / 8) {
+                                a[c] = q[c0 + c];
+                                b[c] = kk[c0 + c];
+                            }
+                        }
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
-                                const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
-                                u = fmaf(fa.x, fb.x, u);
-                                u = fmaf(fa.y, fb.y, u);
+                        for (int c = 0; c < 8; ++c) {
+                            if (c0 + c < p.d / 8) {
+                                const uint32_t aw[4] = {a[c].x, a[c].y, a[c].z, a[c].w};
+                                const uint32_t bw[4] = {b[c].x, b[c].y, b[c].z, b[c].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 fa =
+                                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+                                    const float2 fb =
+                                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+                                    u = fmaf(fa.x, fb.x, u);
+                                    u = fmaf(fa.y, fb.y, u);
+                                }
                             }
                         }
                     }
@@ -546,12 +550,13 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     }
 }
 
-__global__ void __launch_bounds__(256) tc_prep_kernel(const __grid_constant__ TcParams p) {
+// (two blocks per SM: a call's 256 or so slabs then run in one wave)
+__global__ void __launch_bounds__(256, 2) tc_prep_kernel(const __grid_constant__ TcParams p) {
     tc_prep_body(p, blockIdx.x);
 }
 
 // All prompts of a wave: blocks b * S .. b * S + S - 1 prepare prompt b.
-__global__ void __launch_bounds__(256) tc_prep_batch_kernel(const __grid_constant__ TcBatch bt) {
+__global__ void __launch_bounds__(256, 2) tc_prep_batch_kernel(const __grid_constant__ TcBatch bt) {
     const int S = bt.p[0].S;
     tc_prep_body(bt.p[blockIdx.x / S], blockIdx.x % S);
 }
@@ -780,6 +785,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
         float* wref = rbuf + ew * 16;                  // the warp's 16 row references (P1)
         const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * tpg * 16 + rh * 8);
         const int odd = n_tiles & 1;
+        const bool all_rows = p.R == kRP;              // every query row is a real (step, head) row
         int ls = 0, lph = 0;                           // next landing tile of the group's ring, its phase
         int hs1 = 0, hs2 = 0;                          // held slots of the next P1 and P2 slabs
         uint32_t chg = 0;                              // held tiles (hs * tpg + j) whose references P2 reloads
@@ -947,7 +953,12 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     // shared-memory reads overlap the TMEM load
                     float* a = acc_g + (size_t)t * p.N * kTileRows + tok;
                     float av[16 / G];
-                    load_acc<G>(a, rh, p.N, av);
+                    if (all_rows) {
+#pragma unroll
+                        for (int jl = 0; jl < 16 / G; ++jl) av[jl] = a[(rh * (16 / G) + jl) * kTileRows];
+                    } else {
+                        load_acc<G>(a, rh, p.N, av);
+                    }
                     if ((chg >> (hs * tpg + j)) & 1u) {
                         float c[16], l[16];
                         load16(cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16, c);
@@ -964,14 +975,24 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                         y[2 * k + 1] = f.y + d[2 * k + 1];
                     }
                     // rows rh*16 + k are look-ahead steps jj = rh*(16/G) + k/G, heads k%G
+                    if (all_rows) {
 #pragma unroll
-                    for (int jl = 0; jl < 16 / G; ++jl) {
-                        const int jj = rh * (16 / G) + jl;
-                        if (jj < p.N) {
+                        for (int jl = 0; jl < 16 / G; ++jl) {
                             float m = y[jl * G];
 #pragma unroll
                             for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jl * G + hh]);
-                            a[jj * kTileRows] = fmaxf(av[jl], m);
+                            a[(rh * (16 / G) + jl) * kTileRows] = fmaxf(av[jl], m);
+                        }
+                    } else {
+#pragma unroll
+                        for (int jl = 0; jl < 16 / G; ++jl) {
+                            const int jj = rh * (16 / G) + jl;
+                            if (jj < p.N) {
+                                float m = y[jl * G];
+#pragma unroll
+                                for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jl * G + hh]);
+                                a[jj * kTileRows] = fmaxf(av[jl], m);
+                            }
                         }
                     }
                 }
