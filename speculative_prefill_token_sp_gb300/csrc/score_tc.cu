@@ -459,41 +459,19 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     WsHeader* hdr = p.hdr;
     const int l = s / p.H_kv, g = s % p.H_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (p.first && s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
-    if (p.lse_mode) {
-        // the given lse, already published (tag 1) for the fetch warp; padded rows 0
-        if (threadIdx.x < kRP) {
-            const int r = threadIdx.x;
-            float v = 0.f;
-            if (r < p.R) v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N + r / p.G] * 1.4426950408889634f;
-            lse[(size_t)s * kRP + r] = (unsigned long long)__float_as_uint(v) | (1ull << 32);
-        }
-    } else {
-        if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
-        unsigned long long* ps = partials + (size_t)s * kRP * p.Pc;
-        for (int i = threadIdx.x; i < kRP * p.Pc; i += blockDim.x) ps[i] = 0ull;
-    }
-    if (p.F > 1) {
-        // combined running maxima (0 is below every encoded float) and the
-        // per-range arrival counters
-        const size_t n = (size_t)p.N * p.T;
-        for (size_t i = (size_t)s * blockDim.x + threadIdx.x; i < n; i += (size_t)p.S * blockDim.x)
-            p.acc_glob[i] = 0u;
-        for (int i = s * blockDim.x + threadIdx.x; i < p.Pc; i += p.S * blockDim.x) p.arrivals[i] = 0;
-    }
+    // Loads first (the query rows of the image, then the look-ahead dot
+    // products), stores after, so that the load latencies overlap.
     const int cpr = p.d / 8;                      // 16-byte chunks per row
     uint8_t* img = qimg + (size_t)s * kRP * p.d * 2;
-#pragma unroll 2
-    for (int idx = threadIdx.x; idx < kRP * cpr; idx += blockDim.x) {
-        const int r = idx / cpr, ch = idx % cpr;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < p.R) {
+    uint4 iv[2];                                  // at most 32 rows x 16 chunks over 256 threads
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int idx = threadIdx.x + u * (int)blockDim.x, r = idx / cpr, ch = idx % cpr;
+        iv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < kRP * cpr && r < p.R) {
             const int j = r / p.G, h = g * p.G + r % p.G;
-            v = *reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d + ch * 8);
+            iv[u] = *reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d + ch * 8);
         }
-        const int half = ch >> 3, c = ch & 7;
-        const size_t off = (size_t)half * (kRP * 128) + (size_t)r * 128 + (size_t)((c ^ (r & 7)) * 16);
-        *reinterpret_cast<uint4*>(img + off) = v;
     }
     // row r (query j = r / G, head g*G + r % G) against look-ahead keys k <= j - shift:
     // eight consecutive lanes per row, one key each (keys k, k + 8, ... folded
@@ -547,6 +525,37 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
             }
             if (sub == 0) la[(size_t)s * kRP + r] = make_float2(m, z);
         }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int idx = threadIdx.x + u * (int)blockDim.x, r = idx / cpr, ch = idx % cpr;
+        if (idx < kRP * cpr) {
+            const int half = ch >> 3, c = ch & 7;
+            const size_t off = (size_t)half * (kRP * 128) + (size_t)r * 128 + (size_t)((c ^ (r & 7)) * 16);
+            *reinterpret_cast<uint4*>(img + off) = iv[u];
+        }
+    }
+    if (p.first && s == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0;
+    if (p.lse_mode) {
+        // the given lse, already published (tag 1) for the fetch warp; padded rows 0
+        if (threadIdx.x < kRP) {
+            const int r = threadIdx.x;
+            float v = 0.f;
+            if (r < p.R) v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N + r / p.G] * 1.4426950408889634f;
+            lse[(size_t)s * kRP + r] = (unsigned long long)__float_as_uint(v) | (1ull << 32);
+        }
+    } else {
+        if (threadIdx.x < kRP) lse[(size_t)s * kRP + threadIdx.x] = 0ull;
+        unsigned long long* ps = partials + (size_t)s * kRP * p.Pc;
+        for (int i = threadIdx.x; i < kRP * p.Pc; i += blockDim.x) ps[i] = 0ull;
+    }
+    if (p.F > 1) {
+        // combined running maxima (0 is below every encoded float) and the
+        // per-range arrival counters
+        const size_t n = (size_t)p.N * p.T;
+        for (size_t i = (size_t)s * blockDim.x + threadIdx.x; i < n; i += (size_t)p.S * blockDim.x)
+            p.acc_glob[i] = 0u;
+        for (int i = s * blockDim.x + threadIdx.x; i < p.Pc; i += p.S * blockDim.x) p.arrivals[i] = 0;
     }
 }
 
