@@ -114,6 +114,43 @@ def test_varlen_ragged_with_empty_prompts(sp):
             check_importance(got[cu[b]:cu[b + 1]], oracle.importance(r.Q_la, r.K_prompt, r.K_la), "bf16", f"req {b}")
 
 
+def _varlen_parity(sp, v, what):
+    import torch
+    Q, K, Kla, cu = v.packed()
+    n0 = sp.sp_kernel_launches()
+    got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu, check=True)
+    torch.cuda.synchronize()
+    launches = sp.sp_kernel_launches() - n0
+    got = got.cpu().numpy()
+    for b, r in enumerate(v.requests):
+        if r.M:
+            check_importance(got[cu[b]:cu[b + 1]], oracle.importance(r.Q_la, r.K_prompt, r.K_la), "bf16",
+                             f"{what} req {b}")
+    return launches
+
+
+def test_varlen_more_prompts_than_one_wave_holds(sp):
+    """40 short prompts (some empty): a wave takes at most 32 prompts, so the
+    batch runs as two waves of one preparation and one scoring launch each.
+    N*G = 16 < 32 rows also takes P2's bounds-checked path."""
+    wl = W.Workload("t", L=2, H=8, H_kv=2, d=64, M=0, N=4, dtype="bf16", chunk=16, pool_k=1, mode="topk",
+                    keep_rate=0.3, needle_frac=0.05, run_min=2, run_max=8)
+    rng = np.random.default_rng(40)
+    lengths = [int(m) if m > 20 else 0 for m in rng.integers(0, 400, size=40)]
+    assert sum(1 for m in lengths if m) > 32
+    v = W.make_varlen_inputs(wl, 41, lengths=lengths)
+    assert _varlen_parity(sp, v, "40 prompts") == 4
+
+
+def test_varlen_prompts_split_over_waves(sp):
+    """A 120K-token prompt needs 118 of the SMs at 8 tiles per CTA and slab, so
+    the 40K-token one after it starts a second wave (with the 5-token one)."""
+    wl = W.Workload("t", L=1, H=4, H_kv=1, d=64, M=0, N=2, dtype="bf16", chunk=64, pool_k=3, mode="topk",
+                    keep_rate=0.1, needle_frac=0.01, run_min=16, run_max=128)
+    v = W.make_varlen_inputs(wl, 42, lengths=[120000, 40000, 5])
+    assert _varlen_parity(sp, v, "two waves") == 4
+
+
 def test_zero_lookahead_gives_ones_and_empty_prompt_is_noop(sp):
     import torch
     K = torch.randn(2, 2, 50, 64, device="cuda").to(torch.bfloat16)
