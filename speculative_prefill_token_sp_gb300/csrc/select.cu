@@ -112,32 +112,77 @@ __device__ __forceinline__ double token_score(const SelGeo& g, float v, int64_t 
 }
 
 // (1) chunk sums (left to right from 0.0) and means (one divide).
+// Sum (left to right from 0.0) and mean (one divide) of global chunk gc;
+// sixteen loads in flight ahead of the additions.
+__device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __restrict__ imp,
+                                               const float2* __restrict__ mm, int64_t gc, double& sum, double& mean) {
+    const int b = find_batch(g.cn, g.B, gc);
+    const int64_t c = gc - g.cn[b];
+    const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
+    const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
+    const float2 mmb = g.has_boost && g.normalize ? mm[b] : make_float2(0.f, 0.f);
+    double s = 0.0;
+    int64_t i = lo;
+    for (; i + 16 <= hi; i += 16) {
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = imp[m0 + i + k];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) s = __dadd_rn(s, token_score(g, v[k], i + k, Mb, mmb));
+    }
+    for (; i < hi; ++i) s = __dadd_rn(s, token_score(g, imp[m0 + i], i, Mb, mmb));
+    sum = s;
+    mean = __ddiv_rn(s, (double)(hi - lo));
+}
+
 __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const float2* __restrict__ mm,
                              double* __restrict__ sums, double* __restrict__ means, int32_t* __restrict__ hdr) {
     // a fresh status for the call (the workspace header)
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
     const int64_t total = g.cn[g.B];
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
-         gc += (int64_t)gridDim.x * blockDim.x) {
-        const int b = find_batch(g.cn, g.B, gc);
-        const int64_t c = gc - g.cn[b];
-        const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
-        const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
-        const float2 mmb = g.has_boost && g.normalize ? mm[b] : make_float2(0.f, 0.f);
-        // left to right from 0.0; sixteen loads in flight ahead of the additions
-        double s = 0.0;
-        int64_t i = lo;
-        for (; i + 16 <= hi; i += 16) {
-            float v[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = imp[m0 + i + k];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) s = __dadd_rn(s, token_score(g, v[k], i + k, Mb, mmb));
+         gc += (int64_t)gridDim.x * blockDim.x)
+        chunk_sum_mean(g, imp, mm, gc, sums[gc], means[gc]);
+}
+
+// (1+2) chunk sums and means, and the centred pool, for the block's 64 chunks:
+// the means of the block's chunks and of r = (pool_k - 1) / 2 chunks on each
+// side go to shared memory (the halo's are computed again, with the same
+// operations), then each chunk's window, clipped to its own prompt, is summed
+// left to right from 0.0 and divided by its count, as in pool_kernel.
+constexpr int kPoolBlock = 64;
+constexpr int kMaxPoolHalo = 224;        // r at most: the window's means fit in 4 KB
+__global__ void __launch_bounds__(kPoolBlock) chunk_pool_kernel(const SelGeo g, const float* __restrict__ imp,
+                                                                const float2* __restrict__ mm,
+                                                                double* __restrict__ sums, double* __restrict__ means,
+                                                                double* __restrict__ pooled,
+                                                                int32_t* __restrict__ hdr) {
+    __shared__ double win[kPoolBlock + 2 * kMaxPoolHalo];
+    if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
+    const int64_t total = g.cn[g.B];
+    const int r = (g.pool_k - 1) / 2;
+    const int64_t gc0 = (int64_t)blockIdx.x * kPoolBlock;
+    for (int w = threadIdx.x; w < kPoolBlock + 2 * r; w += kPoolBlock) {
+        const int64_t gc = gc0 - r + w;
+        if (gc < 0 || gc >= total) continue;
+        double sm, mn;
+        chunk_sum_mean(g, imp, mm, gc, sm, mn);
+        win[w] = mn;
+        if (w >= r && w < r + kPoolBlock) {
+            sums[gc] = sm;
+            means[gc] = mn;
         }
-        for (; i < hi; ++i) s = __dadd_rn(s, token_score(g, imp[m0 + i], i, Mb, mmb));
-        sums[gc] = s;
-        means[gc] = __ddiv_rn(s, (double)(hi - lo));
     }
+    __syncthreads();
+    const int64_t gc = gc0 + threadIdx.x;
+    if (gc >= total) return;
+    const int b = find_batch(g.cn, g.B, gc);
+    const int64_t c = gc - g.cn[b], nc = g.cn[b + 1] - g.cn[b];
+    const int64_t lo = c - r < 0 ? 0 : c - r;
+    const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
+    double s = 0.0;
+    for (int64_t t = lo; t <= hi; ++t) s = __dadd_rn(s, win[threadIdx.x + r + (t - c)]);
+    pooled[gc] = __ddiv_rn(s, (double)(hi - lo + 1));
 }
 
 // (2) centred average pool over the prompt's own chunks; edges average in-range
@@ -194,7 +239,7 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 // warp-aggregated shared-memory atomics.  The passes stop once every key with
 // the selected prefix is taken.  Then keys above the prefix, and the first
 // `remaining` equal to it in chunk order, are kept.
-__device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double* __restrict__ means, int64_t c0, int nc, int64_t Mb,
+__device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double* __restrict__ keys_src, int64_t c0, int nc, int64_t Mb,
                                   int kc, int* __restrict__ flags, int64_t* __restrict__ offs,
                                   int32_t* __restrict__ kept_b, int64_t* __restrict__ n_kept_b, unsigned* hist,
                                   long long* scan_sh, uint64_t* s_prefix, int* s_remaining, int* s_done) {
@@ -204,7 +249,7 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
 #pragma unroll
     for (int q = 0; q < kRegKeys; ++q) {
         const int c = q * bd + tid;
-        key[q] = c < nc ? order_key(pooled_at(g, means, c0, nc, c)) : 0ull;
+        key[q] = c < nc ? order_key(keys_src[c0 + c]) : 0ull;
     }
     uint64_t prefix = 0, pmask = 0;
     int remaining = kc;
@@ -313,7 +358,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         int kc = (int)ceilf(prod);
         kc = kc < 1 ? 1 : (kc > nc ? nc : kc);
         if (nc <= (int)blockDim.x * kRegKeys) {
-            topk_in_registers(g, means, c0, nc, Mb, kc, flags, offs, kept_pos + g.cu[b], n_kept + b, hist, scan_sh,
+            topk_in_registers(g, g.pool_k > 1 ? pooled : means, c0, nc, Mb, kc, flags, offs, kept_pos + g.cu[b],
+                              n_kept + b, hist, scan_sh,
                               &s_prefix, &s_remaining, &s_done);
             return;
         }
@@ -618,13 +664,20 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     }
     if (total > 0) {
         // small blocks: the fixed-order fp64 sums run on as many SMs as possible
-        const int blocks = (int)std::min<int64_t>((total + 63) / 64, 8192);
         int32_t* hdr = (p.has_boost && p.boost.normalize) ? nullptr : static_cast<int32_t*>(ws);
-        chunk_kernel<<<blocks, 64, 0, st>>>(g, p.importance, mm, sums, means, hdr);
-        SP_LAUNCH_CHECK();
-        if (p.mode == SP_SELECT_TOPK && p.max_nc > (int64_t)kSelThreads * kRegKeys) {
-            pool_kernel<<<(int)std::min<int64_t>((total + 255) / 256, 2048), 256, 0, st>>>(g, means, pooled);
+        const bool pool = p.mode == SP_SELECT_TOPK && p.pool_k > 1;
+        if (pool && (p.pool_k - 1) / 2 <= kMaxPoolHalo) {
+            chunk_pool_kernel<<<(unsigned)((total + kPoolBlock - 1) / kPoolBlock), kPoolBlock, 0, st>>>(
+                g, p.importance, mm, sums, means, pooled, hdr);
             SP_LAUNCH_CHECK();
+        } else {
+            const int blocks = (int)std::min<int64_t>((total + 63) / 64, 8192);
+            chunk_kernel<<<blocks, 64, 0, st>>>(g, p.importance, mm, sums, means, hdr);
+            SP_LAUNCH_CHECK();
+            if (pool) {
+                pool_kernel<<<(int)std::min<int64_t>((total + 255) / 256, 2048), 256, 0, st>>>(g, means, pooled);
+                SP_LAUNCH_CHECK();
+            }
         }
     }
     size_t dyn = 0;

@@ -78,6 +78,8 @@ RANDOM_CASES = [
     (32768, 2, 1, "mass", 0.99, W.CONFIGS[4].boost, 2),
     (5000, 10, 1, "mass", 1.0, None, 0),
     (3000, 16, 3, "topk", 0.4, W.CONFIGS[4].boost, 0),
+    (5000, 1, 101, "topk", 0.1, None, 2),      # wide pool window: 50 chunks of halo per block
+    (3000, 1, 501, "topk", 0.2, None, 0),      # a halo beyond the fused kernel's: the separate pool pass
 ]
 
 
