@@ -149,14 +149,38 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without comments and with whitespace collapsed: a change
+    to comments alone leaves the compiled kernels, and this digest, as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest() -> str:
+    """sha256 of the scoring kernels' code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_prefill_token_sp_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith("score") or name.endswith(".cuh"):
-            with open(os.path.join(csrc, name), "rb") as f:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode())
-                h.update(f.read())
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

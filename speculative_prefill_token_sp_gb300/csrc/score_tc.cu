@@ -8,14 +8,19 @@
 // computed as (1/N) sum_j exp(max_{l,h}(s - lse)) (exp is increasing).
 //
 // Design (one persistent CTA per SM, cooperative launch so that all CTAs are
-// resident).  Every CTA owns one fixed range of prompt tokens (multiples of 32)
-// in every (layer, KV head) slab, so the max over heads and layers of a token
-// stays inside one CTA: no atomics on the data path, and importance is written
-// once.  A row's weights can only be normalised once its lse over all M tokens
-// -- i.e. over every CTA -- is known, so each slab has a statistics pass (P1)
-// and, `lag` slabs later, a normalise pass (P2).  K is read from
-// HBM exactly once; the logits wait for P2 in TMEM.  Warp roles:
-//  * warp 0 (TMA): streams the CTA's K rows (32-row x 128-byte boxes, 128B
+// resident).  The slabs ((layer, KV head) pairs) are dealt to F classes; the
+// CTAs of a class each own one fixed range of prompt tokens (multiples of 32)
+// in every slab of the class, so a token's max over the class's heads and
+// layers stays inside one CTA, and the F CTAs of a range combine their maxima
+// once at the end (order-preserving atomicMax; with F = 1 importance is
+// written directly).  A row's weights can only be normalised once its lse over
+// all M tokens -- i.e. over every CTA of the class -- is known, so each slab
+// has a statistics pass (P1) and, `lag` slabs later, a normalise pass (P2).
+// K is read from HBM exactly once; the logits wait for P2 in TMEM.  A batch of
+// prompts runs in waves: each prompt of a wave gets its own CTAs, plan and
+// workspace slice in one launch (tc_score_batch_kernel).  Warp roles:
+//  * warp 0 (TMA): streams the CTA's K rows (one 128-row x 128-byte box per 64
+//    columns of a full tile, 32-row boxes for a slab's ragged last tile, 128B
 //    swizzle) through a ring of shared-memory stages in plain order (slab after
 //    slab, so every CTA reads one sequential stream), and each slab's query rows
 //    (a pre-swizzled image built by tc_prep_kernel) with one bulk copy;
@@ -40,11 +45,17 @@
 //    writes them to global memory (single 64-bit stores; a published entry
 //    always has z >= 1, so a zeroed entry means "not there yet" and no fence is
 //    needed);
-//  * warps 19-22 (merge): CTA c merges slabs s = c, c + P, ...: it reads every
-//    CTA's entry (re-reading those still 0), adds the look-ahead keys and
-//    publishes lse as (value, tag) 64-bit entries;
+//  * warps 19-22 (merge): a slab is merged by the CTA of its class whose range
+//    index is the slab's position in the class modulo the CTAs per class: it
+//    reads every CTA's entry (re-reading those still 0), adds the look-ahead
+//    keys and publishes lse as (value, tag) 64-bit entries;
 //  * warp 23 (fetch): waits until a slab's lse entries are all tagged and copies
 //    them into a shared-memory ring for the epilogue.
+// The TMA and MMA warps issue from one lane each on SM sub-partitions shared
+// with busy epilogue warps, so their per-tile instruction streams are kept
+// short: inline barrier waits, ring counters instead of divisions, MMA
+// descriptors advanced by constants.  Epilogue warps wait with every lane and a
+// vote, so the common path has no divergent branch.
 //
 // Units: every logit, statistic, lse and running max inside this kernel is in
 // base 2 (the natural-log value times log2 e), so each weight is one exp2; the
