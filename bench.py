@@ -6,7 +6,7 @@ followed by sp_select (chunk mean -> avg pool -> top-K -> position IDs) on one
 synthetic prompt of the Llama-3.1-8B-shaped speculator at M = 32768 tokens
 (L=32, H=32, H_kv=8, d=128, N=8, bf16, chunk 32, pool 3, keep 10%).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--config I]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--workload NAME]
 
 Prints one JSON line (rank 0).  value = prompt tokens scored+selected per second
 over all ranks (each rank runs its own replica: weak scaling), timed with CUDA
@@ -40,7 +40,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", type=int, default=2, help="workload index (default 2: 8B shape, M=32K)")
+    ap.add_argument("--workload", default="llama8b-bf16-32k",
+                    help="single-prompt workload (default: the 8B shape at M = 32K)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bare", action="store_true",
                     help="run only the warm-up and timed steps and print their time (for profilers)")
@@ -253,8 +254,8 @@ def run_reference(args) -> None:
     if rank != 0:
         return
     import workloads as W
-    wl = W.CONFIGS[args.config]
-    x = W.make_inputs(wl, args.config)
+    wl = W.BY_NAME[args.workload]
+    x = W.make_inputs(wl, wl.seed)
     per_step = []
     for k in range(args.warmup + args.steps):
         ts, tsel = oracle_sample(x, 1)
@@ -297,9 +298,9 @@ def run_gpu(args) -> None:
     barrier(world)
     B.build()
     dev = torch.device("cuda", local)
-    wl = W.CONFIGS[args.config]
+    wl = W.BY_NAME[args.workload]
     assert wl.batch == 1, "bench runs a single-prompt workload"
-    x = W.make_inputs(wl, args.config)
+    x = W.make_inputs(wl, wl.seed)
 
     def upload(a):
         if a.dtype == np.uint16:

@@ -33,16 +33,16 @@ import functools  # noqa: E402
 
 
 @functools.lru_cache(maxsize=None)
-def config_inputs(index: int):
+def workload_inputs(name: str):
     import workloads as W
-    return W.make_config_inputs(index)
+    return W.make_workload_inputs(name)
 
 
 @functools.lru_cache(maxsize=None)
-def config_oracle(index: int):
-    """fp64 oracle importance of workload `index` (a list per request for a batch)."""
+def workload_oracle(name: str):
+    """fp64 oracle importance of the named workload (a list per request for a batch)."""
     import oracle
-    x = config_inputs(index)
+    x = workload_inputs(name)
     if hasattr(x, "requests"):
         return [oracle.importance(r.Q_la, r.K_prompt, r.K_la) for r in x.requests]
     return oracle.importance(x.Q_la, x.K_prompt, x.K_la)

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import workloads as W
-from gpu_helpers import check_importance, config_inputs, config_oracle, to_device
+from gpu_helpers import check_importance, to_device, workload_inputs, workload_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -30,11 +30,11 @@ def run_score(sp, x):
     return imp.cpu().numpy()
 
 
-@pytest.mark.parametrize("index", [0, 1, 2, 3])
-def test_config_parity(sp, index):
-    x = config_inputs(index)
+@pytest.mark.parametrize("name", ["tiny-f32-512", "llama8b-bf16-8k", "llama8b-bf16-32k", "llama8b-bf16-128k"])
+def test_workload_parity(sp, name):
+    x = workload_inputs(name)
     got = run_score(sp, x)
-    ref = config_oracle(index)
+    ref = workload_oracle(name)
     check_importance(got, ref, x.wl.dtype, x.wl.name)
 
 
@@ -42,7 +42,7 @@ def test_tensor_core_path_serves_the_8b_workloads(sp):
     """The 8B-shaped bf16 prompts run on the tcgen05 path: one preparation
     kernel plus one persistent kernel per call (the general path launches 4)."""
     import torch
-    x = config_inputs(1)
+    x = workload_inputs("llama8b-bf16-8k")
     Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
     n0 = sp.sp_kernel_launches()
     sp.score(Q, K, Kla)
@@ -50,14 +50,14 @@ def test_tensor_core_path_serves_the_8b_workloads(sp):
     assert sp.sp_kernel_launches() - n0 == 2
 
 
-def test_varlen_config_parity(sp):
+def test_varlen_v3_batch_parity(sp):
     import torch
-    v = config_inputs(4)
+    v = workload_inputs("v3-batch16-0.8b-bf16")
     Q, K, Kla, cu = v.packed()
     got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu, check=True)
     torch.cuda.synchronize()
     got = got.cpu().numpy()
-    refs = config_oracle(4)
+    refs = workload_oracle("v3-batch16-0.8b-bf16")
     for b, r in enumerate(v.requests):
         ref = refs[b]
         check_importance(got[cu[b]:cu[b + 1]], ref, v.wl.dtype, f"{v.wl.name} request {b}")
@@ -169,7 +169,7 @@ def test_zero_lookahead_gives_ones_and_empty_prompt_is_noop(sp):
 
 def test_workspace_status_ok_after_call(sp):
     import torch
-    x = W.make_config_inputs(0)
+    x = W.make_workload_inputs("tiny-f32-512")
     Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
     wl = x.wl
     need = sp.sp_score_workspace_size(wl.L, wl.H, wl.H_kv, wl.d, wl.M, wl.N, sp.SP_F32)

@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 import workloads as W
-from gpu_helpers import check_importance, config_inputs, to_device
+from gpu_helpers import check_importance, to_device, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -44,9 +44,9 @@ def check_case(sp, x, what):
     check_importance(got, ref, x.wl.dtype, what)
 
 
-@pytest.mark.parametrize("index", [0, 1])
-def test_config_parity(sp, index):
-    x = config_inputs(index)
+@pytest.mark.parametrize("name", ["tiny-f32-512", "llama8b-bf16-8k"])
+def test_workload_parity(sp, name):
+    x = workload_inputs(name)
     check_case(sp, x, x.wl.name)
 
 

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import workloads as W
-from gpu_helpers import config_inputs, config_oracle, to_device
+from gpu_helpers import to_device, workload_inputs, workload_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -37,20 +37,20 @@ def assert_same(sp, imp, chunk, pool_k, mode, rate, boost=None):
     assert got.shape[0] == n and np.array_equal(got, want), (chunk, pool_k, mode, rate, got[:20], want[:20])
 
 
-@pytest.mark.parametrize("index", [0, 1, 2, 3])
-def test_config_selection_bit_exact(sp, index):
+@pytest.mark.parametrize("name", ["tiny-f32-512", "llama8b-bf16-8k", "llama8b-bf16-32k", "llama8b-bf16-128k"])
+def test_workload_selection_bit_exact(sp, name):
     """Oracle importance (rounded to fp32) -> GPU selection == oracle selection."""
-    x = config_inputs(index)
+    x = workload_inputs(name)
     wl = x.wl
-    imp = config_oracle(index).astype(np.float32)
+    imp = workload_oracle(name).astype(np.float32)
     assert_same(sp, imp, wl.chunk, wl.pool_k, wl.mode, wl.keep_rate)
 
 
 def test_v3_batch_selection_bit_exact(sp):
     import torch
-    v = config_inputs(4)
+    v = workload_inputs("v3-batch16-0.8b-bf16")
     wl = v.wl
-    imps = [r.astype(np.float32) for r in config_oracle(4)]
+    imps = [r.astype(np.float32) for r in workload_oracle("v3-batch16-0.8b-bf16")]
     packed = np.concatenate(imps)
     got = sp.select_varlen(torch.from_numpy(packed).cuda(), v.cu_M, wl.chunk, wl.pool_k, wl.mode, wl.mass,
                            wl.boost)
@@ -72,12 +72,12 @@ RANDOM_CASES = [
     (65537, 32, 3, "topk", 0.1, None, 0),
     (300000, 64, 3, "topk", 0.2, None, 5),
     (9, 4, 1, "mass", 0.85, None, 0),
-    (150, 32, 1, "mass", 0.85, W.CONFIGS[4].boost, 0),
+    (150, 32, 1, "mass", 0.85, W.V3_BOOST, 0),
     (2000, 32, 1, "mass", 0.5, (64, 1.5, 128, 1.3, 0), 3),
-    (20000, 32, 1, "mass", 0.85, W.CONFIGS[4].boost, 0),
-    (32768, 2, 1, "mass", 0.99, W.CONFIGS[4].boost, 2),
+    (20000, 32, 1, "mass", 0.85, W.V3_BOOST, 0),
+    (32768, 2, 1, "mass", 0.99, W.V3_BOOST, 2),
     (5000, 10, 1, "mass", 1.0, None, 0),
-    (3000, 16, 3, "topk", 0.4, W.CONFIGS[4].boost, 0),
+    (3000, 16, 3, "topk", 0.4, W.V3_BOOST, 0),
     (5000, 1, 101, "topk", 0.1, None, 2),      # wide pool window: 50 chunks of halo per block
     (3000, 1, 501, "topk", 0.2, None, 0),      # a halo beyond the fused kernel's: the separate pool pass
 ]
@@ -96,7 +96,7 @@ def test_random_selection_bit_exact(sp, case):
 def test_constant_importance_keeps_first_chunks(sp):
     imp = np.full(1000, 0.125, dtype=np.float32)
     assert_same(sp, imp, 32, 3, "topk", 0.3)
-    assert_same(sp, imp, 32, 1, "mass", 0.85, W.CONFIGS[4].boost)
+    assert_same(sp, imp, 32, 1, "mass", 0.85, W.V3_BOOST)
 
 
 def test_empty_and_varlen_edges(sp):
@@ -105,7 +105,7 @@ def test_empty_and_varlen_edges(sp):
     lens = [0, 1, 33, 0, 500, 64]
     cu = np.concatenate([[0], np.cumsum(lens)])
     imp = rng.random(int(cu[-1])).astype(np.float32)
-    for mode, rate, pool, boost in (("topk", 0.3, 3, None), ("mass", 0.7, 1, W.CONFIGS[4].boost)):
+    for mode, rate, pool, boost in (("topk", 0.3, 3, None), ("mass", 0.7, 1, W.V3_BOOST)):
         got = sp.select_varlen(torch.from_numpy(imp).cuda(), cu, 16, pool, mode, rate, boost)
         torch.cuda.synchronize()
         want = oracle.select_varlen(imp, cu, 16, pool, mode, rate, boost)
@@ -113,19 +113,19 @@ def test_empty_and_varlen_edges(sp):
             assert np.array_equal(got[b].cpu().numpy(), want[b][0]), (mode, b)
 
 
-@pytest.mark.parametrize("index", [0, 1, 2])
-def test_end_to_end_pipeline(sp, index):
+@pytest.mark.parametrize("name", ["tiny-f32-512", "llama8b-bf16-8k", "llama8b-bf16-32k"])
+def test_end_to_end_pipeline(sp, name):
     """GPU importance -> GPU selection: the count follows the kc rule exactly and
     every disagreement with the oracle's selection is a near-tie."""
     import torch
-    x = config_inputs(index)
+    x = workload_inputs(name)
     wl = x.wl
     Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
     imp_gpu = sp.score(Q, K, Kla)
     kept = sp.select(imp_gpu, wl.chunk, wl.pool_k, wl.mode, wl.keep_rate)
     torch.cuda.synchronize()
     kept = kept.cpu().numpy()
-    ref_imp = config_oracle(index)
+    ref_imp = workload_oracle(name)
     want, n = oracle.select(ref_imp.astype(np.float32), wl.chunk, wl.pool_k, wl.mode, wl.keep_rate)
     assert kept.shape[0] == n                   # same kc, and all chunks are full here
     assert np.all(np.diff(kept) > 0)

@@ -5,9 +5,9 @@ import workloads as W
 
 
 def test_deterministic_and_shapes():
-    a = W.make_config_inputs(0)
-    b = W.make_config_inputs(0)
-    wl = W.CONFIGS[0]
+    a = W.make_workload_inputs("tiny-f32-512")
+    b = W.make_workload_inputs("tiny-f32-512")
+    wl = W.BY_NAME["tiny-f32-512"]
     assert a.Q_la.shape == (wl.N, wl.L, wl.H, wl.d)
     assert a.K_prompt.shape == (wl.L, wl.H_kv, wl.M, wl.d)
     assert a.K_la.shape == (wl.L, wl.H_kv, wl.N, wl.d)
@@ -17,7 +17,7 @@ def test_deterministic_and_shapes():
 
 
 def test_needle_runs_fraction():
-    wl = W.CONFIGS[1]
+    wl = W.BY_NAME["llama8b-bf16-8k"]
     rng = np.random.default_rng(0)
     pos = W.needle_positions(rng, wl, wl.M)
     assert pos.size >= round(0.05 * wl.M) and pos.size < round(0.05 * wl.M) + wl.run_max
@@ -37,7 +37,7 @@ def test_bf16_rounding_ties_to_even():
 
 
 def test_varlen_packing():
-    wl = W.CONFIGS[4]
+    wl = W.BY_NAME["v3-batch16-0.8b-bf16"]
     v = W.make_varlen_inputs(wl, 4, lengths=[5, 0, 9])
     Q, K, Kla, cu = v.packed()
     assert cu.tolist() == [0, 5, 5, 14]

@@ -36,8 +36,8 @@ from typing import Optional
 import numpy as np
 
 __all__ = [
-    "CONFIGS", "Workload", "Inputs", "VarlenInputs", "make_inputs",
-    "make_varlen_inputs", "make_config_inputs", "bf16_bits_from_f32",
+    "WORKLOADS", "BY_NAME", "V3_BOOST", "Workload", "Inputs", "VarlenInputs", "make_inputs",
+    "make_varlen_inputs", "make_workload_inputs", "bf16_bits_from_f32",
     "f32_from_bf16_bits", "needle_positions",
 ]
 
@@ -66,6 +66,7 @@ class Workload:
     run_max: int = 0
     batch: int = 1
     M_min: int = 0              # batch: prompt lengths uniform in [M_min, M]
+    seed: int = 0               # the workload's own seed for its inputs
 
     @property
     def G(self) -> int:
@@ -76,25 +77,28 @@ class Workload:
         return self.L * self.H_kv * self.d * (4 if self.dtype == "f32" else 2)
 
 
-# The five workloads.  Index = seed.
-CONFIGS = [
+# The five workloads, each with its own seed.
+WORKLOADS = [
     Workload("tiny-f32-512", L=2, H=4, H_kv=2, d=64, M=512, N=4, dtype="f32",
              chunk=32, pool_k=3, mode="topk", keep_rate=0.3,
-             needle_kind="single", needle_count=16),
+             needle_kind="single", needle_count=16, seed=0),
     Workload("llama8b-bf16-8k", L=32, H=32, H_kv=8, d=128, M=8192, N=8, dtype="bf16",
              chunk=32, pool_k=3, mode="topk", keep_rate=0.3,
-             needle_frac=0.05, run_min=8, run_max=64),
+             needle_frac=0.05, run_min=8, run_max=64, seed=1),
     Workload("llama8b-bf16-32k", L=32, H=32, H_kv=8, d=128, M=32768, N=8, dtype="bf16",
              chunk=32, pool_k=3, mode="topk", keep_rate=0.1,
-             needle_frac=0.02, run_min=16, run_max=128),
+             needle_frac=0.02, run_min=16, run_max=128, seed=2),
     Workload("llama8b-bf16-128k", L=32, H=32, H_kv=8, d=128, M=131072, N=8, dtype="bf16",
              chunk=64, pool_k=3, mode="topk", keep_rate=0.1,
-             needle_frac=0.01, run_min=16, run_max=128),
+             needle_frac=0.01, run_min=16, run_max=128, seed=3),
     Workload("v3-batch16-0.8b-bf16", L=24, H=16, H_kv=4, d=64, M=32768, N=8, dtype="bf16",
              chunk=32, pool_k=1, mode="mass", mass=0.85,
              boost=(64, 1.5, 128, 1.3, 1),
-             needle_frac=0.05, run_min=8, run_max=64, batch=16, M_min=2048),
+             needle_frac=0.05, run_min=8, run_max=64, batch=16, M_min=2048, seed=4),
 ]
+BY_NAME = {w.name: w for w in WORKLOADS}
+# the v3 structural boosts: first 64 tokens x1.5, last 128 x1.3, scores min-max normalised first
+V3_BOOST = BY_NAME["v3-batch16-0.8b-bf16"].boost
 
 
 # ---------------------------------------------------------------------------
@@ -240,9 +244,9 @@ def make_varlen_inputs(wl: Workload, seed: int, lengths=None) -> VarlenInputs:
     return VarlenInputs(wl, reqs, cu)
 
 
-def make_config_inputs(index: int):
-    """Inputs of workload ``index`` with its own seed (= index)."""
-    wl = CONFIGS[index]
+def make_workload_inputs(name: str):
+    """Inputs of the named workload, drawn with its own seed."""
+    wl = BY_NAME[name]
     if wl.batch > 1:
-        return make_varlen_inputs(wl, index)
-    return make_inputs(wl, index)
+        return make_varlen_inputs(wl, wl.seed)
+    return make_inputs(wl, wl.seed)
