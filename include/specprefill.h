@@ -169,7 +169,10 @@ sp_status sp_score_lse(const void* Q_la, const void* K_prompt, const float* lse,
                        int L, int H, int H_kv, int d, int64_t M, int N, sp_dtype dtype,
                        float* importance, void* ws, size_t ws_bytes, void* stream);
 
-/* Workspace bytes for sp_score_varlen (cu_M_host: B+1 host prefix sums). */
+/* Workspace bytes for sp_score_varlen (cu_M_host: B+1 host prefix sums).  The
+ * batch is planned for the current device's SM count: query the size with the
+ * device that will run the call current (a smaller workspace is rejected with
+ * SP_EINVAL, never overrun). */
 size_t sp_score_varlen_workspace_size(int B, const int64_t* cu_M_host, int L, int H, int H_kv,
                                       int d, int N, sp_dtype dtype);
 
