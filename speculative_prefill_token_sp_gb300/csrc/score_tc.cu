@@ -110,7 +110,7 @@ constexpr int kRing = 16;            // entries of the lse ring
 constexpr int kStatsRing = 4;        // entries of the statistics ring
 constexpr int kMaxQ = 4;             // query-image buffers
 constexpr int kMaxLand = 4;          // landing tiles per epilogue group
-constexpr int kMaxClasses = 8;       // slab classes, at most
+constexpr int kMaxClasses = 16;      // slab classes, at most
 constexpr int kMinClassTokens = 768; // tokens per CTA per slab that need no further classes
 constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024;
