@@ -14,11 +14,17 @@
 // mass in ranked order -- so the result equals any IEEE-754 evaluation of the
 // same steps bit for bit.
 //
-// Kernels: (0) per-prompt min/max (normalisation only), (1) chunk sums and
-// means, (2) pooled scores (top-K mode), (3) one CTA per prompt: radix select
-// of exactly kc chunks on (score desc, index asc), or a bitonic sort of
-// (mean desc, index asc) and the running-mass cut; then the exclusive scan of
-// kept chunk sizes, (4) compaction of the kept positions.
+// Kernels: (0) per-prompt min/max (normalisation only); (1+2) chunk sums and
+// means with the pooled scores in one multi-block pass (chunk_pool_kernel:
+// each block pools its chunks from a shared-memory window with a halo), or
+// chunk sums (1) and a separate pool pass (2) for windows wider than the halo;
+// (3) one CTA per prompt: radix select of exactly kc chunks on (score desc,
+// index asc) with the keys in registers (prompts of up to 4096 chunks; longer
+// ones read them from memory each pass), or a bitonic sort of (mean desc,
+// index asc) and the running-mass cut; then the exclusive scan of kept chunk
+// sizes and, for chunks of up to 256 tokens, the kept positions themselves;
+// (4) compaction of the kept positions for larger chunks or longer prompts;
+// (5) the guide's v2 keep rules (sp_select_rules).
 #include "sp_common.cuh"
 
 #include <math.h>

@@ -63,3 +63,14 @@ def test_single_process_needs_no_process_group():
     assert total_ms == 8.0 and value == pytest.approx(1000 * 4 / 0.008)
     assert bench.max_over_ranks(3.0, 1) == 3.0
     bench.barrier(1)
+
+
+def test_kernel_digest_ignores_comments_and_whitespace():
+    """The DRAM-traffic record is keyed to the scoring kernels' code: comment and
+    whitespace edits leave the key unchanged, code edits (even inside string
+    literals) change it."""
+    import bench
+    base = 'int a = 1;  // note\n/* block */ asm("x // y");\n'
+    assert bench._code_only(base) == bench._code_only('int a = 1;\n\n   asm("x // y");  // other note\n')
+    assert bench._code_only(base) != bench._code_only(base.replace("a = 1", "a = 2"))
+    assert bench._code_only(base) != bench._code_only(base.replace("x // y", "x // z"))
