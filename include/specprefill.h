@@ -191,6 +191,28 @@ sp_status sp_score_varlen(const void* Q_la, const void* K_prompt, const void* K_
                           int L, int H, int H_kv, int d, int N, sp_dtype dtype,
                           float* importance, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes for sp_score_lse_varlen (planned for the current device, as
+ * sp_score_varlen_workspace_size; 0 if the shape or cu_M_host is invalid). */
+size_t sp_score_lse_varlen_workspace_size(int B, const int64_t* cu_M_host, int L, int H, int H_kv,
+                                          int d, int N, sp_dtype dtype);
+
+/* sp_score_lse for B independent prompts in one call: the packing of
+ * sp_score_varlen, with each prompt's row normalisers given instead of its
+ * look-ahead keys (single pass per prompt, K read once).
+ *
+ *   Q_la      [B, N, L, H, d]
+ *   K_prompt  [L, H_kv, T, d]   T = cu_M_host[B]; prompt b occupies rows cu_M[b]..cu_M[b+1]-1
+ *   lse       [B, L, H, N]      fp32 natural-log normalisers of prompt b's rows (device, 4-byte aligned)
+ *   importance[T]               fp32; entries of prompt b at offsets cu_M[b]..
+ *
+ * Same definition as sp_score_lse per prompt; requirements and errors as
+ * sp_score_varlen.  lse holds all B prompts' rows; those of empty prompts are
+ * not used. */
+sp_status sp_score_lse_varlen(const void* Q_la, const void* K_prompt, const float* lse,
+                              int B, const int64_t* cu_M_host,
+                              int L, int H, int H_kv, int d, int N, sp_dtype dtype,
+                              float* importance, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Selection                                                                */
 /* ------------------------------------------------------------------------ */

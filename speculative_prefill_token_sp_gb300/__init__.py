@@ -20,11 +20,12 @@ __all__ = [
     "sp_score_workspace_size", "sp_score", "sp_score_lse_workspace_size", "sp_score_lse",
     "sp_score_prefill_workspace_size", "sp_score_prefill",
     "sp_score_varlen_workspace_size", "sp_score_varlen",
+    "sp_score_lse_varlen_workspace_size", "sp_score_lse_varlen",
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
     "sp_select_noalloc", "sp_select_rules_workspace_size", "sp_select_rules", "SpKeepRules", "GUIDE_RULES",
     "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
     "sp_kernel_launches",
-    "score", "score_lse", "score_prefill", "score_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
+    "score", "score_lse", "score_prefill", "score_varlen", "score_lse_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
 ]
 
 SP_OK, SP_EINVAL, SP_ENOMEM, SP_ECUDA, SP_EDEVICE, SP_ETIMEOUT, SP_EUNSUPPORTED = range(7)
@@ -74,6 +75,9 @@ _SIGS = {
     "sp_score_varlen_workspace_size": (_sz, [_i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32]),
     "sp_score_varlen": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
                                _sz, _vp]),
+    "sp_score_lse_varlen_workspace_size": (_sz, [_i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "sp_score_lse_varlen": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                   _sz, _vp]),
     "sp_select_workspace_size": (_sz, [_i64, _i32]),
     "sp_select": (_i32, [_vp, _i64, _i32, _i32, _i32, _dbl, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sp_select_varlen_workspace_size": (_sz, [_i32, _vp, _i32]),
@@ -187,6 +191,18 @@ def sp_score_varlen(Q_la, K_prompt, K_la, B, cu_M_host, L, H, H_kv, d, N, dtype,
     cu = _i64_array(cu_M_host)
     return lib().sp_score_varlen(_ptr(Q_la), _ptr(K_prompt), _ptr(K_la), B, ctypes.addressof(cu), L, H, H_kv,
                                  d, N, dtype, _ptr(importance), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def sp_score_lse_varlen_workspace_size(B, cu_M_host, L, H, H_kv, d, N, dtype) -> int:
+    cu = _i64_array(cu_M_host)
+    return lib().sp_score_lse_varlen_workspace_size(B, ctypes.addressof(cu), L, H, H_kv, d, N, dtype)
+
+
+def sp_score_lse_varlen(Q_la, K_prompt, lse, B, cu_M_host, L, H, H_kv, d, N, dtype, importance, ws, ws_bytes,
+                        stream=None) -> int:
+    cu = _i64_array(cu_M_host)
+    return lib().sp_score_lse_varlen(_ptr(Q_la), _ptr(K_prompt), _ptr(lse), B, ctypes.addressof(cu), L, H,
+                                     H_kv, d, N, dtype, _ptr(importance), _ptr(ws), ws_bytes, _stream(stream))
 
 
 def sp_select_workspace_size(M, chunk) -> int:
@@ -357,6 +373,24 @@ def score_varlen(Q_la, K_prompt, K_la, cu_M, *, importance=None, ws=None, stream
     ws = _workspace(need, K_prompt.device, ws)
     _check(sp_score_varlen(Q_la, K_prompt, K_la, B, cu, L, H, H_kv, d, N, dt, importance, ws, ws.numel(),
                            stream))
+    _check_device(ws, stream, check)
+    return importance
+
+
+def score_lse_varlen(Q_la, K_prompt, lse, cu_M, *, importance=None, ws=None, stream=None, check=False):
+    """Packed importance [T] of B prompts from given row normalisers: Q_la [B,N,L,H,d],
+    K_prompt [L,H_kv,T,d], lse [B,L,H,N] fp32 (device)."""
+    import torch
+    B, N, L, H, d = Q_la.shape
+    H_kv, T = K_prompt.shape[1], K_prompt.shape[2]
+    cu = [int(x) for x in cu_M]
+    dt = _dtype_code(K_prompt)
+    if importance is None:
+        importance = torch.empty(T, dtype=torch.float32, device=K_prompt.device)
+    need = sp_score_lse_varlen_workspace_size(B, cu, L, H, H_kv, d, N, dt)
+    ws = _workspace(need, K_prompt.device, ws)
+    _check(sp_score_lse_varlen(Q_la, K_prompt, lse, B, cu, L, H, H_kv, d, N, dt, importance, ws, ws.numel(),
+                               stream))
     _check_device(ws, stream, check)
     return importance
 

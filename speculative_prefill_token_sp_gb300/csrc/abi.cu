@@ -359,6 +359,30 @@ sp_status sp_score_varlen(const void* Q_la, const void* K_prompt, const void* K_
     return run_score("sp_score_varlen", p, ws, ws_bytes, stream);
 }
 
+size_t sp_score_lse_varlen_workspace_size(int B, const int64_t* cu_M_host, int L, int H, int H_kv, int d,
+                                          int N, sp_dtype dtype) {
+    if (check_cu("sp_score_lse_varlen_workspace_size", B, cu_M_host) != SP_OK) return 0;
+    if (check_shape("sp_score_lse_varlen_workspace_size", L, H, H_kv, d, N, dtype) != SP_OK) return 0;
+    ScoreProblem p = make_score_problem(nullptr, nullptr, nullptr, B, cu_M_host, L, H, H_kv, d, N, dtype,
+                                        nullptr);
+    p.lse_mode = true;
+    return score_ws(p);
+}
+
+sp_status sp_score_lse_varlen(const void* Q_la, const void* K_prompt, const float* lse, int B,
+                              const int64_t* cu_M_host, int L, int H, int H_kv, int d, int N,
+                              sp_dtype dtype, float* importance, void* ws, size_t ws_bytes, void* stream) {
+    sp_status s = check_cu("sp_score_lse_varlen", B, cu_M_host);
+    if (s != SP_OK) return s;
+    s = check_shape("sp_score_lse_varlen", L, H, H_kv, d, N, dtype);
+    if (s != SP_OK) return s;
+    ScoreProblem p = make_score_problem(Q_la, K_prompt, nullptr, B, cu_M_host, L, H, H_kv, d, N, dtype,
+                                        importance);
+    p.lse_in = lse;
+    p.lse_mode = true;
+    return run_score("sp_score_lse_varlen", p, ws, ws_bytes, stream);
+}
+
 sp_status sp_gather_kept(const int32_t* token_ids, int B, const int64_t* cu_M_host, const int32_t* kept_pos,
                          const int64_t* n_kept, int32_t* out_tokens, int32_t* out_positions, int64_t* cu_kept,
                          void* stream) {

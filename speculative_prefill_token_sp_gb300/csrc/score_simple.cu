@@ -194,16 +194,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Geo geo, const 
     }
 }
 
-// (2') lse given by the caller (one prompt): lse_in[l, h, j] into this path's
-// [slab, row] layout, row r = j*G + h % G of slab l*H_kv + h / G.
+// (2') lse given by the caller: lse_in[b, l, h, j] into this path's [slab, row]
+// layout, row r = j*G + h % G of slab (b*L + l)*H_kv + h / G.
 __global__ void lse_in_kernel(const Geo geo, const float* __restrict__ lse_in, float* __restrict__ lse) {
-    const int64_t n = (int64_t)geo.L * geo.H_kv * geo.R;
+    const int64_t n = (int64_t)geo.B * geo.L * geo.H_kv * geo.R;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t sl = i / geo.R;
         const int r = (int)(i % geo.R);
-        const int l = (int)(sl / geo.H_kv), g = (int)(sl % geo.H_kv);
+        const int64_t bl = sl / geo.H_kv;           // b*L + l
+        const int g = (int)(sl % geo.H_kv);
         const int j = r / geo.G, h = g * geo.G + r % geo.G;
-        lse[i] = lse_in[((int64_t)l * geo.H + h) * geo.N + j];
+        lse[i] = lse_in[(bl * geo.H + h) * geo.N + j];
     }
 }
 

@@ -1432,6 +1432,7 @@ void bind_prompt(const ScoreProblem& q, int b, bool first, uint8_t* ws, uint8_t*
     p.Qp = static_cast<const __nv_bfloat16*>(q.Q) + (size_t)b * q.N * q.L * q.H * q.d;
     p.Klap = q.Kla ? static_cast<const __nv_bfloat16*>(q.Kla) + (size_t)b * q.L * q.H_kv * (q.N - q.la_shift) * q.d
                    : nullptr;
+    p.lse_in = q.lse_in ? q.lse_in + (size_t)b * q.L * q.H * q.N : nullptr;   // [B, L, H, N]
 }
 
 // Waves of a batch: consecutive non-empty prompts, at most kMaxWave of them,

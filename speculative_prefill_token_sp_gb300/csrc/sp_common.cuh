@@ -43,7 +43,7 @@ struct ScoreProblem {
     const void* Q;          // [B, N, L, H, d]
     const void* K;          // [L, H_kv, T, d]
     const void* Kla;        // [B, L, H_kv, N, d]; unused when lse_in is given
-    const float* lse_in;    // [L, H, N] softmax normalisers given by the caller (lse_mode)
+    const float* lse_in;    // [B, L, H, N] softmax normalisers given by the caller (lse_mode)
     bool lse_mode;          // sp_score_lse: lse_in replaces the statistics pass
     int la_shift;           // row j sees look-ahead keys 0..j-la_shift (1: row 0 is the prefill's last query);
                             // K_la holds N - la_shift keys per (layer, KV head)

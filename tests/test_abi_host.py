@@ -152,3 +152,21 @@ def test_score_prefill_validation(sp):
     assert f(16, 16, 16, 2, 4, 2, 64, 512, 200, sp.SP_F32, 16, 16, need, 0) == sp.SP_EUNSUPPORTED  # (N+1)*G > 256
     assert f(16, 16, 16, 2, 4, 2, 64, 512, 3, sp.SP_F32, 16, 16, need - 1, 0) == sp.SP_ENOMEM
     assert f(16, 16, None, 2, 4, 2, 64, 512, 3, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL       # keys needed
+
+
+def test_score_lse_varlen_validation(sp):
+    """sp_score_lse_varlen: the offsets rules of sp_score_varlen, the lse pointer rules of sp_score_lse."""
+    cu = [0, 300, 300, 812]
+    need = sp.sp_score_lse_varlen_workspace_size(3, cu, 2, 4, 2, 64, 4, sp.SP_F32)
+    assert need > 0
+    assert sp.sp_score_lse_varlen_workspace_size(3, [0, 300, 200, 812], 2, 4, 2, 64, 4, sp.SP_F32) == 0
+    assert sp.sp_score_lse_varlen_workspace_size(3, cu, 2, 5, 2, 64, 4, sp.SP_F32) == 0     # H % H_kv != 0
+    f = sp.sp_score_lse_varlen
+    assert f(16, 16, 16, 3, [1, 300, 300, 812], 2, 4, 2, 64, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL
+    assert f(16, 16, 16, 3, cu, 2, 4, 2, 12, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EUNSUPPORTED   # d
+    assert f(16, 16, 16, 3, cu, 2, 4, 2, 64, 4, sp.SP_F32, 16, 16, need - 1, 0) == sp.SP_ENOMEM
+    assert f(16, 16, None, 3, cu, 2, 4, 2, 64, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL       # null lse
+    assert f(16, 16, 18, 3, cu, 2, 4, 2, 64, 4, sp.SP_F32, 16, 16, need, 0) == sp.SP_EINVAL         # misaligned lse
+    assert "aligned" in sp.sp_last_error()
+    cu257 = list(range(0, 258))
+    assert f(16, 16, 16, 257, cu257, 2, 4, 2, 64, 4, sp.SP_F32, 16, 16, 1 << 30, 0) == sp.SP_EUNSUPPORTED

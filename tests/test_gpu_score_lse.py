@@ -84,3 +84,59 @@ def test_zero_lookahead_gives_ones(sp):
     imp = sp.score_lse(Q, K, lse)
     torch.cuda.synchronize()
     assert torch.all(imp == 1.0)
+
+
+def _lse_varlen_parity(sp, v, what):
+    """sp_score_lse_varlen on a packed batch against the oracle prompt by prompt;
+    returns the number of kernels the call launched."""
+    import torch
+    Q, K, _, cu = v.packed()
+    lse32 = np.stack([oracle.row_lse(r.Q_la, r.K_prompt, r.K_la) for r in v.requests]).astype(np.float32)
+    n0 = sp.sp_kernel_launches()
+    got = sp.score_lse_varlen(to_device(Q), to_device(K), torch.from_numpy(lse32).cuda(), cu, check=True)
+    torch.cuda.synchronize()
+    launches = sp.sp_kernel_launches() - n0
+    got = got.cpu().numpy()
+    for b, r in enumerate(v.requests):
+        if r.M:
+            ref = oracle.importance_given_lse(r.Q_la, r.K_prompt, lse32[b].astype(np.float64))
+            check_importance(got[cu[b]:cu[b + 1]], ref, v.wl.dtype, f"{what} req {b}")
+    return launches
+
+
+def test_varlen_v3_batch_parity(sp):
+    """The 16-request 0.8B-shaped batch (2K to 32K tokens each) in one call."""
+    _lse_varlen_parity(sp, workload_inputs("v3-batch16-0.8b-bf16"), "v3 batch")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_varlen_ragged_with_empty_prompts(sp, dt):
+    """Empty, one-token and ragged prompts; bf16 on the tensor-core path, fp32
+    on the general path."""
+    wl = W.Workload("t", L=2, H=8, H_kv=2, d=64, M=0, N=4, dtype=dt, chunk=16, pool_k=1, mode="mass",
+                    mass=0.85, needle_frac=0.05, run_min=2, run_max=8)
+    v = W.make_varlen_inputs(wl, 78, lengths=[300, 0, 1, 129, 1000, 0])
+    _lse_varlen_parity(sp, v, f"ragged {dt}")
+
+
+def test_varlen_more_prompts_than_one_wave_holds(sp):
+    """40 short prompts: two waves of one preparation and one scoring launch each."""
+    wl = W.Workload("t", L=2, H=8, H_kv=2, d=128, M=0, N=4, dtype="bf16", chunk=16, pool_k=1, mode="topk",
+                    keep_rate=0.3, needle_frac=0.05, run_min=2, run_max=8)
+    rng = np.random.default_rng(43)
+    lengths = [int(m) if m > 20 else 0 for m in rng.integers(0, 400, size=40)]
+    assert sum(1 for m in lengths if m) > 32
+    v = W.make_varlen_inputs(wl, 44, lengths=lengths)
+    assert _lse_varlen_parity(sp, v, "40 prompts") == 4
+
+
+def test_varlen_one_prompt_equals_single_call(sp):
+    """A batch of one prompt gives bit-identical importance to sp_score_lse."""
+    import torch
+    x = workload_inputs("llama8b-bf16-8k")
+    lse = torch.from_numpy(oracle.row_lse(x.Q_la, x.K_prompt, x.K_la).astype(np.float32)).cuda()
+    Q, K = to_device(x.Q_la), to_device(x.K_prompt)
+    a = sp.score_lse(Q, K, lse)
+    b = sp.score_lse_varlen(Q[None], K, lse[None], [0, x.wl.M])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
