@@ -432,6 +432,31 @@ __device__ __forceinline__ void load_acc(const float* a, int rh, int N, float (&
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// y = f32(h) + c for both halves h of a packed fp16 pair: the mixed-precision
+// add of sm_100 and later, one instruction per half.  The widening is exact,
+// so the result is the fp32 sum rounded once, as with a conversion first.
+__device__ __forceinline__ void add_h2_f32(uint32_t h2, float c0, float c1, float& y0, float& y1) {
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+        : "=f"(y0), "=f"(y1) : "r"(h2), "f"(c0), "f"(c1));
+}
+
+// max(a, b, c) in one instruction (three-input max of sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// m = max(m, y[0], ..., y[G-1])
+template <int G>
+__device__ __forceinline__ float fold_heads(float m, const float* y) {
+#pragma unroll
+    for (int hh = 0; hh + 1 < G; hh += 2) m = fmax3(m, y[hh], y[hh + 1]);
+    if (G & 1) m = fmaxf(m, y[G - 1]);
+    return m;
+}
+
 // Order-preserving 32-bit code of a float (a < b  <=>  code(a) < code(b) as
 // unsigned), so that atomicMax on codes takes the max of floats; 0 is below
 // the code of every float.
@@ -841,11 +866,10 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     for (int jl = 0; jl < 16 / G; ++jl) {
                         const int jj = rh * (16 / G) + jl;
                         if (jj < p.N) {
-                            float m = fmaf(x[jl * G], p.scale_log2e, -lr[jl * G]);
+                            float y[G];
 #pragma unroll
-                            for (int hh = 1; hh < G; ++hh)
-                                m = fmaxf(m, fmaf(x[jl * G + hh], p.scale_log2e, -lr[jl * G + hh]));
-                            a[jj * kTileRows] = fmaxf(a[jj * kTileRows], m);
+                            for (int hh = 0; hh < G; ++hh) y[hh] = fmaf(x[jl * G + hh], p.scale_log2e, -lr[jl * G + hh]);
+                            a[jj * kTileRows] = fold_heads<G>(a[jj * kTileRows], y);
                         }
                     }
                 }
@@ -905,10 +929,11 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     for (int r = 0; r < 16; ++r) o[r] = fmaf(x[r], p.scale_log2e, -ref[r]);
                     bool redo;
                     if (have_ref) {
-                        float om[4] = {o[0], o[1], o[2], o[3]};
-#pragma unroll
-                        for (int k = 4; k < 16; ++k) om[k & 3] = fmaxf(om[k & 3], o[k]);
-                        redo = __any_sync(0xffffffffu, valid && fmaxf(fmaxf(om[0], om[1]), fmaxf(om[2], om[3])) > kRefMargin);
+                        const float m0 = fmax3(o[0], o[1], o[2]), m1 = fmax3(o[3], o[4], o[5]);
+                        const float m2 = fmax3(o[6], o[7], o[8]), m3 = fmax3(o[9], o[10], o[11]);
+                        const float m4 = fmax3(o[12], o[13], o[14]);
+                        const float om = fmaxf(fmax3(m0, m1, m2), fmax3(m3, m4, o[15]));
+                        redo = __any_sync(0xffffffffu, valid && om > kRefMargin);
                     } else {
                         redo = __any_sync(0xffffffffu, valid);
                     }
@@ -989,30 +1014,17 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     tmem_ld8_wait(pk);
                     float y[16];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
-                        y[2 * k] = f.x + d[2 * k];
-                        y[2 * k + 1] = f.y + d[2 * k + 1];
-                    }
+                    for (int k = 0; k < 8; ++k) add_h2_f32(pk[k], d[2 * k], d[2 * k + 1], y[2 * k], y[2 * k + 1]);
                     // rows rh*16 + k are look-ahead steps jj = rh*(16/G) + k/G, heads k%G
                     if (all_rows) {
 #pragma unroll
-                        for (int jl = 0; jl < 16 / G; ++jl) {
-                            float m = y[jl * G];
-#pragma unroll
-                            for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jl * G + hh]);
-                            a[(rh * (16 / G) + jl) * kTileRows] = fmaxf(av[jl], m);
-                        }
+                        for (int jl = 0; jl < 16 / G; ++jl)
+                            a[(rh * (16 / G) + jl) * kTileRows] = fold_heads<G>(av[jl], y + jl * G);
                     } else {
 #pragma unroll
                         for (int jl = 0; jl < 16 / G; ++jl) {
                             const int jj = rh * (16 / G) + jl;
-                            if (jj < p.N) {
-                                float m = y[jl * G];
-#pragma unroll
-                                for (int hh = 1; hh < G; ++hh) m = fmaxf(m, y[jl * G + hh]);
-                                a[jj * kTileRows] = fmaxf(av[jl], m);
-                            }
+                            if (jj < p.N) a[jj * kTileRows] = fold_heads<G>(av[jl], y + jl * G);
                         }
                     }
                 }
