@@ -155,10 +155,12 @@ __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, cons
 // the means of the block's chunks and of r = (pool_k - 1) / 2 chunks on each
 // side go to shared memory (the halo's are computed again, with the same
 // operations), then each chunk's window, clipped to its own prompt, is summed
-// left to right from 0.0 and divided by its count, as in pool_kernel.
+// left to right from 0.0 and divided by its count, as in pool_kernel.  The
+// block has a thread for each of its 64 + 2r means (rounded up to whole warps),
+// so every mean is one thread's single chain of additions.
 constexpr int kPoolBlock = 64;
 constexpr int kMaxPoolHalo = 224;        // r at most: the window's means fit in 4 KB
-__global__ void __launch_bounds__(kPoolBlock) chunk_pool_kernel(const SelGeo g, const float* __restrict__ imp,
+__global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kernel(const SelGeo g, const float* __restrict__ imp,
                                                                 const float2* __restrict__ mm,
                                                                 double* __restrict__ sums, double* __restrict__ means,
                                                                 double* __restrict__ pooled,
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kPoolBlock) chunk_pool_kernel(const SelGeo g, 
     const int64_t total = g.cn[g.B];
     const int r = (g.pool_k - 1) / 2;
     const int64_t gc0 = (int64_t)blockIdx.x * kPoolBlock;
-    for (int w = threadIdx.x; w < kPoolBlock + 2 * r; w += kPoolBlock) {
+    for (int w = threadIdx.x; w < kPoolBlock + 2 * r; w += blockDim.x) {
         const int64_t gc = gc0 - r + w;
         if (gc < 0 || gc >= total) continue;
         double sm, mn;
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kPoolBlock) chunk_pool_kernel(const SelGeo g, 
     }
     __syncthreads();
     const int64_t gc = gc0 + threadIdx.x;
-    if (gc >= total) return;
+    if (threadIdx.x >= kPoolBlock || gc >= total) return;
     const int b = find_batch(g.cn, g.B, gc);
     const int64_t c = gc - g.cn[b], nc = g.cn[b + 1] - g.cn[b];
     const int64_t lo = c - r < 0 ? 0 : c - r;
@@ -673,7 +675,8 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
         int32_t* hdr = (p.has_boost && p.boost.normalize) ? nullptr : static_cast<int32_t*>(ws);
         const bool pool = p.mode == SP_SELECT_TOPK && p.pool_k > 1;
         if (pool && (p.pool_k - 1) / 2 <= kMaxPoolHalo) {
-            chunk_pool_kernel<<<(unsigned)((total + kPoolBlock - 1) / kPoolBlock), kPoolBlock, 0, st>>>(
+            const int threads = (kPoolBlock + (p.pool_k - 1) + 31) / 32 * 32;     // 64 + 2r means, whole warps
+            chunk_pool_kernel<<<(unsigned)((total + kPoolBlock - 1) / kPoolBlock), threads, 0, st>>>(
                 g, p.importance, mm, sums, means, pooled, hdr);
             SP_LAUNCH_CHECK();
         } else {
