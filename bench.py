@@ -12,6 +12,13 @@ Prints one JSON line (rank 0).  value = prompt tokens scored+selected per second
 over all ranks (each rank runs its own replica: weak scaling), timed with CUDA
 events on the launching stream, inputs resident in HBM; the K cache (2 GiB) is
 far larger than L2 and L2 is also flushed between timed steps.
+
+Beside the headline, `per_workload` times the other workloads of the path the
+same way (L2 flushed before every call, median of the calls): the 8B shape at
+8K and 128K tokens, the 16-request v3 batch (sp_score_varlen +
+sp_select_varlen) and the tiny fp32 case, each with its fraction of the
+measured HBM bandwidth.  `--impl reference` times the fp64 oracle on the host
+cores, one whole prompt (all layers) per timed step.
 """
 from __future__ import annotations
 
@@ -43,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="llama8b-bf16-32k",
                     help="single-prompt workload (default: the 8B shape at M = 32K)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the other workloads' timings (8K, 128K, the v3 batch, tiny)")
     ap.add_argument("--bare", action="store_true",
                     help="run only the warm-up and timed steps and print their time (for profilers)")
     return ap.parse_args(argv)
@@ -250,30 +259,151 @@ def _slice_layers(x, start, n):
 
 
 def run_reference(args) -> None:
+    """The reference arm: the fp64 oracle on the host cores, one whole step
+    (scoring over all layers + selection of the full prompt) per timed step;
+    the untimed warm-ups run one layer only."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import workloads as W
     wl = W.BY_NAME[args.workload]
     x = W.make_inputs(wl, wl.seed)
+    for _ in range(args.warmup):
+        oracle_sample(x, 1)
     per_step = []
-    for k in range(args.warmup + args.steps):
-        ts, tsel = oracle_sample(x, 1)
-        if k >= args.warmup:
-            per_step.append(ts * wl.L + tsel)
+    for _ in range(args.steps):
+        ts, tsel = oracle_sample(x, wl.L)
+        per_step.append(ts + tsel)
     ms = statistics.mean(per_step) * 1e3
     value = wl.M / (ms / 1e3)
+    sample = (f"each timed step runs the oracle on the whole {wl.name} prompt (all {wl.L} layers of scoring "
+              f"and the full selection); the {args.warmup} untimed warm-ups run 1 layer")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": wl.name, "M": wl.M, "L": wl.L, "H": wl.H, "H_kv": wl.H_kv, "d": wl.d,
                        "N": wl.N, "chunk": wl.chunk, "pool_k": wl.pool_k, "keep_rate": wl.keep_rate,
-                       "sample": "each step times 1 layer of scoring and the full selection, scaled to "
-                                 f"{wl.L} layers"},
+                       "sample": sample, "extrapolated_from_layers": None},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": f"1 of {wl.L} layers per step, scaled"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the other workloads of the path, timed the same way (reported beside the headline)
+# ----------------------------------------------------------------------------
+
+def upload(a, dev):
+    """A generated array on the device: uint16 arrays are bf16 bit patterns."""
+    import numpy as np
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+PER_WORKLOAD = ("tiny-f32-512", "llama8b-bf16-8k", "llama8b-bf16-128k", "v3-batch16-0.8b-bf16")
+
+
+def time_workload(sp, name: str, dev, flush, stream, reps: int, peak: float) -> dict:
+    """One step of the named workload (sp_score + sp_select, or the varlen pair
+    for a batch) and its scoring call alone, each `reps` times with L2 flushed
+    before every call; median milliseconds per step and per scoring call."""
+    import numpy as np
+    import torch
+
+    import workloads as W
+
+    wl = W.BY_NAME[name]
+    x = W.make_workload_inputs(name)
+    dt = sp.SP_BF16 if wl.dtype == "bf16" else sp.SP_F32
+    rate = wl.keep_rate if wl.mode == "topk" else wl.mass
+    mode = sp.SP_SELECT_TOPK if wl.mode == "topk" else sp.SP_SELECT_MASS
+    if wl.batch > 1:
+        Qh, Kh, Klah, cu = x.packed()
+        cu = [int(v) for v in cu]
+        B, T = len(cu) - 1, cu[-1]
+        Q, K, Kla = upload(Qh, dev), upload(Kh, dev), upload(Klah, dev)
+        del Qh, Kh, Klah
+        imp = torch.empty(T, dtype=torch.float32, device=dev)
+        kept = torch.empty(T, dtype=torch.int32, device=dev)
+        n_kept = torch.empty(B, dtype=torch.int64, device=dev)
+        ws_s_bytes = sp.sp_score_varlen_workspace_size(B, cu, wl.L, wl.H, wl.H_kv, wl.d, wl.N, dt)
+        ws_k_bytes = sp.sp_select_varlen_workspace_size(B, cu, wl.chunk)
+        ws_s = torch.empty(ws_s_bytes, dtype=torch.uint8, device=dev)
+        ws_k = torch.empty(ws_k_bytes, dtype=torch.uint8, device=dev)
+
+        def score_call():
+            s = sp.sp_score_varlen(Q, K, Kla, B, cu, wl.L, wl.H, wl.H_kv, wl.d, wl.N, dt, imp, ws_s, ws_s_bytes,
+                                   stream)
+            if s != sp.SP_OK:
+                raise sp.SpError(s, sp.sp_last_error())
+
+        def select_call():
+            s = sp.sp_select_varlen(imp, B, cu, wl.chunk, wl.pool_k, mode, rate, wl.boost, kept, n_kept, ws_k,
+                                    ws_k_bytes, stream)
+            if s != sp.SP_OK:
+                raise sp.SpError(s, sp.sp_last_error())
+    else:
+        T = wl.M
+        Q, K, Kla = upload(x.Q_la, dev), upload(x.K_prompt, dev), upload(x.K_la, dev)
+        imp = torch.empty(T, dtype=torch.float32, device=dev)
+        kept = torch.empty(T, dtype=torch.int32, device=dev)
+        n_kept = torch.empty(1, dtype=torch.int64, device=dev)
+        ws_s_bytes = sp.sp_score_workspace_size(wl.L, wl.H, wl.H_kv, wl.d, T, wl.N, dt)
+        ws_k_bytes = sp.sp_select_workspace_size(T, wl.chunk)
+        ws_s = torch.empty(ws_s_bytes, dtype=torch.uint8, device=dev)
+        ws_k = torch.empty(ws_k_bytes, dtype=torch.uint8, device=dev)
+
+        def score_call():
+            s = sp.sp_score(Q, K, Kla, wl.L, wl.H, wl.H_kv, wl.d, T, wl.N, dt, imp, ws_s, ws_s_bytes, stream)
+            if s != sp.SP_OK:
+                raise sp.SpError(s, sp.sp_last_error())
+
+        def select_call():
+            s = sp.sp_select(imp, T, wl.chunk, wl.pool_k, mode, rate, wl.boost, kept, n_kept, ws_k, ws_k_bytes,
+                             stream)
+            if s != sp.SP_OK:
+                raise sp.SpError(s, sp.sp_last_error())
+    del x
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for k in range(reps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            fn()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    def step():
+        score_call()
+        select_call()
+
+    for _ in range(3):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = sp.sp_workspace_status(ws_s, stream)
+    if st != sp.SP_OK:
+        raise sp.SpError(st, sp.sp_last_error())
+    l0 = sp.sp_kernel_launches()
+    score_call()
+    torch.cuda.synchronize()
+    score_launches = sp.sp_kernel_launches() - l0
+    step_ms = timed(step)
+    score_ms = timed(score_call)
+    k_bytes = wl.k_bytes_per_token() * T
+    achieved = k_bytes / (score_ms / 1e3) / 1e9
+    out = {"tokens": T, "prompts": wl.batch, "ms": step_ms, "tokens_per_s": T / (step_ms / 1e3),
+           "launch_ms": score_ms, "launches_per_call": score_launches, "algorithmic_bytes": k_bytes,
+           "achieved_gbs": achieved, "frac": achieved / peak, "traffic": recorded_traffic(name),
+           "timing": f"median of {reps} steps and of {reps} scoring calls, L2 flushed before each"}
+    del Q, K, Kla, imp, kept, n_kept, ws_s, ws_k
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -302,12 +432,7 @@ def run_gpu(args) -> None:
     assert wl.batch == 1, "bench runs a single-prompt workload"
     x = W.make_inputs(wl, wl.seed)
 
-    def upload(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(a).to(dev)
-
-    Q, K, Kla = upload(x.Q_la), upload(x.K_prompt), upload(x.K_la)
+    Q, K, Kla = upload(x.Q_la, dev), upload(x.K_prompt, dev), upload(x.K_la, dev)
     dt = sp.SP_BF16 if wl.dtype == "bf16" else sp.SP_F32
     M = wl.M
     imp = torch.empty(M, dtype=torch.float32, device=dev)
@@ -432,6 +557,12 @@ def run_gpu(args) -> None:
         kc = max(1, math.ceil(float(np.float32(nc) * np.float32(wl.keep_rate))))
         assert int(h_n.item()) <= kc * wl.chunk
 
+    per_workload = None
+    if rank == 0 and not args.no_per_workload:
+        del hQ, hK, hKla
+        per_workload = {n: time_workload(sp, n, dev, flush, stream, max(5, min(args.steps, 20)), peak)
+                        for n in PER_WORKLOAD if n != wl.name}
+
     if rank != 0:
         barrier(world)
         return
@@ -454,6 +585,8 @@ def run_gpu(args) -> None:
         "gpu_launches": per_step_launches * args.steps,
         "clocks": clk,
     }
+    if per_workload is not None:
+        line["per_workload"] = per_workload
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x)
     print(json.dumps(line), flush=True)

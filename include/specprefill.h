@@ -345,6 +345,22 @@ int sp_version(void);
  * (all entry points, all threads).  For accounting in benchmarks. */
 uint64_t sp_kernel_launches(void);
 
+/* ------------------------------------------------------------------------ */
+/* Test hook (not for production use)                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Sets the limit, in nanoseconds, of the tensor-core scoring kernel's waits
+ * on other CTAs' exchange entries (each token range's softmax statistics and
+ * each row's lse); 0 restores the default of 4 s.  Returns the previous limit.
+ * Calls enqueued afterwards use the new limit (it is read when a call is
+ * planned); waits inside one CTA and the drain of its in-flight copies and
+ * MMAs keep 4 s.  Tests lower it to about a microsecond so that an exchange
+ * wait runs out: the kernel then records SP_ETIMEOUT in the workspace, stops
+ * every warp role, waits for its in-flight copies and MMAs, frees its tensor
+ * memory and returns, and sp_workspace_status reports SP_ETIMEOUT.  Process-
+ * wide, not synchronised with calls running on other threads. */
+uint64_t sp_test_set_exchange_wait_ns(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

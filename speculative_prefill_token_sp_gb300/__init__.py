@@ -24,7 +24,7 @@ __all__ = [
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
     "sp_select_noalloc", "sp_select_rules_workspace_size", "sp_select_rules", "SpKeepRules", "GUIDE_RULES",
     "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
-    "sp_kernel_launches",
+    "sp_kernel_launches", "sp_test_set_exchange_wait_ns",
     "score", "score_lse", "score_prefill", "score_varlen", "score_lse_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
 ]
 
@@ -91,6 +91,7 @@ _SIGS = {
     "sp_status_string": (_c.c_char_p, [_i32]),
     "sp_version": (_i32, []),
     "sp_kernel_launches": (_c.c_uint64, []),
+    "sp_test_set_exchange_wait_ns": (_c.c_uint64, [_c.c_uint64]),
 }
 
 
@@ -277,6 +278,12 @@ def sp_version() -> int:
 
 def sp_kernel_launches() -> int:
     return lib().sp_kernel_launches()
+
+
+def sp_test_set_exchange_wait_ns(ns: int) -> int:
+    """Test hook: limit (ns) of the scoring kernel's waits on other CTAs' exchange
+    entries; 0 restores the default.  Returns the previous limit."""
+    return lib().sp_test_set_exchange_wait_ns(int(ns))
 
 
 # ----------------------------------------------------------------------------

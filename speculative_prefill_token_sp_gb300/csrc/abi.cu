@@ -42,6 +42,7 @@ sp_status gather_launch(const int32_t* token_ids, int B, const int64_t* cu_M_hos
 bool score_tc_supported(const ScoreProblem& p);
 size_t score_tc_ws_bytes(const ScoreProblem& p);
 sp_status score_tc_launch(const ScoreProblem& p, void* ws, cudaStream_t st);
+unsigned long long score_tc_set_exchange_wait_ns(unsigned long long ns);
 
 }  // namespace sp
 
@@ -511,5 +512,7 @@ const char* sp_status_string(sp_status s) {
 int sp_version(void) { return 100; }
 
 uint64_t sp_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+uint64_t sp_test_set_exchange_wait_ns(uint64_t ns) { return score_tc_set_exchange_wait_ns(ns); }
 
 }  // extern "C"

@@ -84,6 +84,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace sp {
@@ -116,6 +117,12 @@ constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
 
+// Limit of the waits on other CTAs' exchange entries (the merge warps' reads
+// of the statistics partials, the fetch warp's reads of lse): kTimeoutNs
+// unless a test lowers it (sp_test_set_exchange_wait_ns).  The waits inside
+// a CTA, and the drain of its in-flight copies and MMAs, always keep kTimeoutNs.
+std::atomic<unsigned long long> g_exchange_wait_ns{kTimeoutNs};
+
 struct TcParams {
     int L, H, H_kv, G, N, R, d;
     int S;              // slabs = L * H_kv
@@ -139,6 +146,7 @@ struct TcParams {
     int la_shift;       // row j sees look-ahead keys 0..j - la_shift
     const float* lse_in;  // [L, H, N] natural-log softmax normalisers (lse_mode)
     float scale, scale_log2e;
+    unsigned long long xwait_ns;    // limit of a wait on other CTAs' exchange entries
     // shared-memory carve (byte offsets from the 1024-aligned base)
     int off_q, off_acc, off_c, off_ref, off_stats, off_lse, off_bar, smem_bytes;
     // workspace
@@ -1142,7 +1150,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     for (int k = 0; k < 16; ++k)
                         if (base + 4 * k < p.Pc && (v[k] >> 32) == 0ull) missing = true;
                     if (!missing) break;
-                    if (*abort_flag || global_ns() - t0 > kTimeoutNs) { ok = false; break; }
+                    if (*abort_flag || global_ns() - t0 > p.xwait_ns) { ok = false; break; }
                     __nanosleep(64);
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
@@ -1195,7 +1203,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                 int stop = 0;
                 if (lane == 0) {
                     if (*abort_flag) stop = 1;
-                    else if (global_ns() - t0 > kTimeoutNs) {
+                    else if (global_ns() - t0 > p.xwait_ns) {
                         record_error(p.hdr, SP_ETIMEOUT, 11);
                         *abort_flag = 1;
                         stop = 1;
@@ -1322,6 +1330,7 @@ bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
     if (p.held * p.tiles_per_group > 32) return false;   // one bit per held tile
     p.scale = 1.0f / sqrtf((float)q.d);
     p.scale_log2e = p.scale * 1.4426950408889634f;
+    p.xwait_ns = g_exchange_wait_ns.load(std::memory_order_relaxed);
     const int stage_bytes = kTileRows * q.d * 2;
     const int q_bytes = kRP * q.d * 2;
     const int n_bars = 2 * 8 + 2 * kMaxQ + 4 * kMaxLand + 2 * kStatsRing + 2 * kRing + 2;
@@ -1512,6 +1521,10 @@ bool plan_waves(const ScoreProblem& q, int sms, std::vector<Wave>& waves) {
 bool use_waves(const ScoreProblem& q) { return q.B > 1; }
 
 }  // namespace
+
+unsigned long long score_tc_set_exchange_wait_ns(unsigned long long ns) {
+    return g_exchange_wait_ns.exchange(ns == 0 ? kTimeoutNs : ns);
+}
 
 bool score_tc_supported(const ScoreProblem& q) {
     Plan plan;

@@ -170,3 +170,11 @@ def test_score_lse_varlen_validation(sp):
     assert "aligned" in sp.sp_last_error()
     cu257 = list(range(0, 258))
     assert f(16, 16, 16, 257, cu257, 2, 4, 2, 64, 4, sp.SP_F32, 16, 16, 1 << 30, 0) == sp.SP_EUNSUPPORTED
+
+
+def test_exchange_wait_hook_is_host_only(sp):
+    """The test hook only stores the limit that later calls read when planned."""
+    prev = sp.sp_test_set_exchange_wait_ns(1234)
+    assert prev == 4_000_000_000
+    assert sp.sp_test_set_exchange_wait_ns(0) == 1234
+    assert sp.sp_test_set_exchange_wait_ns(prev) == 4_000_000_000
