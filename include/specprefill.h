@@ -285,16 +285,20 @@ sp_status sp_select_varlen(const float* importance, int B, const int64_t* cu_M_h
  * the whole device), and plug-ins that a host framework hands only input and
  * output buffers.  The caller passes inputs and outputs exactly as for
  * sp_select; the scratch lives in a fixed 3 MiB array of device memory inside
- * the library, which every GPU that loads the library holds until the process
- * exits.  Nothing is allocated or freed.
+ * the library.  The array comes into being on a device when the library's
+ * code is loaded there: with CUDA's lazy module loading (the default) that is
+ * the first call of this entry point on the device, which looks up the
+ * array's address with that device current and may itself allocate device
+ * memory (the array and the selection kernels' code).  So make one call on
+ * every device ahead of time -- before the allocator or out-of-memory path
+ * that needs it, and before any stream capture.  Later calls allocate and
+ * free nothing; the array stays until the process exits.
  *
  * Limits: one prompt, at most 65536 chunks (ceil(M / chunk)); larger requests
  * return SP_EUNSUPPORTED before any work is enqueued.  All calls on a device
  * share the array and leave their contents behind: calls whose work may
  * overlap on the GPU (e.g. on two unordered streams) race and must not be
- * issued.  The first call on each device looks up the array's address with
- * that device current; make it before any stream capture.  Results are
- * identical to sp_select's. */
+ * issued.  Results are identical to sp_select's. */
 sp_status sp_select_noalloc(const float* importance, int64_t M, int chunk, int pool_k, sp_mode mode,
                             double rate, const sp_boost* boost, int32_t* kept_pos, int64_t* n_kept,
                             void* stream);

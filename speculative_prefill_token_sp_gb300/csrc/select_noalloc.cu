@@ -13,14 +13,17 @@
 // Limits and sharing:
 //  * one prompt per call, at most kNoAllocMaxChunks chunks (ceil(M / chunk));
 //    larger requests are rejected with SP_EUNSUPPORTED before any work;
-//  * the array (kNoAllocScratchBytes) exists on every GPU that loads the
-//    library and stays allocated until the process exits;
+//  * the array (kNoAllocScratchBytes) comes into being on a device when this
+//    file's module is loaded there.  With CUDA's lazy module loading that is
+//    the first call on the device: its cudaGetSymbolAddress (made with that
+//    device current) loads the module, which may allocate device memory for
+//    the array and the kernels' code.  Callers inside an allocator or an
+//    out-of-memory handler must therefore make one call on every device ahead
+//    of time (and before any stream capture); later calls allocate nothing,
+//    and the array stays until the process exits;
 //  * every call on a device uses the same array and leaves its contents
 //    behind; each call clears what it needs cleared, but two calls whose work
-//    overlaps on the GPU (different streams, no ordering) race on it;
-//  * the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture.
+//    overlaps on the GPU (different streams, no ordering) race on it.
 #include "sp_common.cuh"
 
 #include <mutex>

@@ -5,12 +5,15 @@ that must not call cudaMalloc, and plug-ins handed only their input and output
 buffers cannot provide sp_select's workspace.  sp_select_noalloc keeps that
 scratch in a fixed device array inside the library.  These tests call it
 through the C ABI twice in a row (the second call must not see the first
-call's leftovers) and compare with sp_select, which uses a caller workspace;
-selection is integer work, so the comparison is exact.  This file is collected
-last on purpose.
+call's leftovers) and compare with sp_select, which uses a caller workspace,
+and with the oracle's selection of the same importance vector; selection is
+integer work, so the comparisons are exact.  A call after the first one must
+not change the device's free memory.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -59,11 +62,31 @@ def test_no_alloc_matches_workspace_entry_point_twice(sp):
         (20000, 32, 1, sp.SP_SELECT_MASS, 0.85, (64, 1.5, 128, 1.3, 1)),
     ]
     for M, chunk, pool_k, mode, rate, boost in calls:
-        imp = torch.from_numpy((rng.random(M) * 1e-3).astype(np.float32)).cuda()
+        host = (rng.random(M) * 1e-3).astype(np.float32)
+        imp = torch.from_numpy(host).cuda()
         want, n_want = _with_workspace(sp, imp, chunk, pool_k, mode, rate, boost)
         got, n_got = _no_alloc(sp, imp, chunk, pool_k, mode, rate, boost)
         assert n_got == n_want
         assert np.array_equal(got, want)
+        ref, n_ref = oracle.select(host, chunk, pool_k, "topk" if mode == sp.SP_SELECT_TOPK else "mass", rate,
+                                   boost)
+        assert n_got == n_ref and np.array_equal(got, ref)
+
+
+def test_no_alloc_call_leaves_free_device_memory_unchanged(sp):
+    import torch
+    M, chunk = 40000, 32
+    imp = torch.from_numpy((np.random.default_rng(7).random(M) * 1e-3).astype(np.float32)).cuda()
+    kept = torch.empty(M, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int64, device="cuda")
+    # the first call on the device may load the library's module (and its array)
+    assert sp.sp_select_noalloc(imp, M, chunk, 3, sp.SP_SELECT_TOPK, 0.1, None, kept, n) == sp.SP_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    assert sp.sp_select_noalloc(imp, M, chunk, 3, sp.SP_SELECT_TOPK, 0.1, None, kept, n) == sp.SP_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
 
 
 def test_no_alloc_rejects_requests_beyond_its_fixed_scratch(sp):
