@@ -80,6 +80,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <vector>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -896,33 +897,34 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                 }
                 // Statistics of query row rh*16 + r over this quadrant's tokens,
                 // relative to a reference ref[r] that the whole warp shares: each
-                // tile's exp(s - ref) are summed over the 32 lanes and added to
-                // the row's running sum (lanes 2r, 2r + 1).  The reference starts at
-                // the row's maximum over the slab's first tile with a valid token
-                // and rises to a tile's maximum whenever a logit exceeds it by more
-                // than kRefMargin (the sums so far are then rescaled).  It is
-                // always a logit of the row, so z >= 1 once a token was valid, and
-                // the held fp16 offsets s - ref stay at most kRefMargin above 0.
-                // Row maxima and sums go through a shuffle butterfly, and a tile's
-                // references are stored for P2 only when they change: shared
-                // memory is slow while the MMA reads its operands.
+                // lane adds its token's exp(s - ref) of every row to its own
+                // running sums zacc[r], and the 32 lanes' sums of a row are added
+                // once, at the end of the slab (lanes 2r, 2r + 1).  The reference
+                // starts at the row's maximum over the slab's first tile with a
+                // valid token and rises to a tile's maximum whenever a logit
+                // exceeds it by more than kRefMargin (every lane's sums of that
+                // row are then rescaled).  It is always a logit of the row, so
+                // z >= 1 once a token was valid, and the held fp16 offsets s - ref
+                // stay at most kRefMargin above 0.  Row maxima go through a
+                // shuffle butterfly, and a tile's references are stored for P2
+                // only when they change: shared memory is slow while the MMA
+                // reads its operands.
                 float ref_lane = 0.f;                  // ref of row rh*16 + (lane >> 1); all 16 in wref
-                float z_lane = 0.f;                    // and that row's sum of exp(s - ref)
-                bool have_ref = false;
+                float zacc[16];                        // this lane's sums of exp(s - ref), per row
+#pragma unroll
+                for (int r = 0; r < 16; ++r) zacc[r] = 0.f;
                 chg &= ~(((1u << tpg) - 1u) << (hs * tpg));
-                for (int t = t0, j = 0; t < n_tiles; t += 2, ++j) {
+                // One tile of P1, specialised at compile time for the slab's first
+                // tile of this group (it sets the references: no comparison, no
+                // rescale) and for full tiles (every lane's token is valid), so
+                // the common case -- a later, full tile -- carries no per-value
+                // selects or flags.
+                auto p1_tile = [&](auto first_c, auto full_c, int t, int j) -> bool {
+                    constexpr bool kFirst = decltype(first_c)::value, kFull = decltype(full_c)::value;
                     const int slot = grp * p.land + ls;
                     float ref[16];                     // read while the landing tile is awaited
-                    if (have_ref) {
-                        load16(wref, ref);
-                    } else {
-#pragma unroll
-                        for (int r = 0; r < 16; ++r) ref[r] = 0.f;
-                    }
-                    if (!warp_wait(smem_u32(&land_full[slot]), lph, abort_flag, p.hdr, 6)) {
-                        ok = false;
-                        break;
-                    }
+                    if constexpr (!kFirst) load16(wref, ref);
+                    if (!warp_wait(smem_u32(&land_full[slot]), lph, abort_flag, p.hdr, 6)) return false;
                     tc_fence_after();
                     float x[16];
                     tmem_ld16f(tmem_base + lane_addr + (uint32_t)(slot * kRP + rh * 16), x);
@@ -930,39 +932,41 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&land_empty[slot]));    // this part is read
                     if (++ls == p.land) { ls = 0; lph ^= 1; }
-                    const bool valid = t * kTileRows + tok < len;
-                    const bool full_tile = (t + 1) * kTileRows <= len;
+                    const bool valid = kFull || t * kTileRows + tok < len;
                     float o[16];
+                    bool redo = true;
+                    if constexpr (kFirst) {
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) o[r] = fmaf(x[r], p.scale_log2e, -ref[r]);
-                    bool redo;
-                    if (have_ref) {
+                        for (int r = 0; r < 16; ++r) o[r] = x[r] * p.scale_log2e;
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) o[r] = fmaf(x[r], p.scale_log2e, -ref[r]);
                         const float m0 = fmax3(o[0], o[1], o[2]), m1 = fmax3(o[3], o[4], o[5]);
                         const float m2 = fmax3(o[6], o[7], o[8]), m3 = fmax3(o[9], o[10], o[11]);
                         const float m4 = fmax3(o[12], o[13], o[14]);
                         const float om = fmaxf(fmax3(m0, m1, m2), fmax3(m3, m4, o[15]));
-                        redo = __any_sync(0xffffffffu, valid && om > kRefMargin);
-                    } else {
-                        redo = __any_sync(0xffffffffu, valid);
+                        redo = __any_sync(0xffffffffu, (kFull || valid) && om > kRefMargin);
                     }
                     if (redo) {
-                        // each reference rises by its row's largest offset (or starts at it)
+                        // each reference starts at its row's largest value (first
+                        // tile) or rises by the row's largest offset
                         const float mx = warp_rows16<true>(o, valid);   // finite: a lane is valid
-                        const float dm = have_ref ? fmaxf(mx, 0.f) : mx;
-                        ref_lane += dm;
-                        z_lane = have_ref ? z_lane * ex2_approx(-dm) : 0.f;
+                        if constexpr (kFirst) {
+                            ref_lane = mx;
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) o[r] -= __shfl_sync(0xffffffffu, dm, 2 * r);
+                            for (int r = 0; r < 16; ++r) o[r] -= __shfl_sync(0xffffffffu, mx, 2 * r);
+                        } else {
+                            const float dm = fmaxf(mx, 0.f);
+                            ref_lane += dm;
+                            const float f = ex2_approx(-dm);   // rescale of the row's sums
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                o[r] -= __shfl_sync(0xffffffffu, dm, 2 * r);
+                                zacc[r] *= __shfl_sync(0xffffffffu, f, 2 * r);
+                            }
+                        }
                         if ((lane & 1) == 0) wref[lane >> 1] = ref_lane;
                         __syncwarp();
-                        have_ref = true;
-                    }
-                    if (have_ref) {
-                        float e[16];
-#pragma unroll
-                        for (int r = 0; r < 16; ++r) e[r] = ex2_approx(o[r]);
-                        // (the lanes past the range occur only in a ragged last tile)
-                        z_lane += full_tile ? warp_rows16<false>(e, true) : warp_rows16<false>(e, valid);
                     }
                     uint32_t pk[8];
 #pragma unroll
@@ -970,7 +974,15 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                         const __half2 h2 = __floats2half2_rn(o[2 * k], o[2 * k + 1]);
                         pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
-                    if (j == 0 || redo) {
+                    if constexpr (kFull) {
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) zacc[r] += ex2_approx(o[r]);
+                    } else {
+                        // (the lanes past the range occur only in a ragged last tile)
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) zacc[r] += valid ? ex2_approx(o[r]) : 0.f;
+                    }
+                    if (redo) {
                         // the tile's fp16 references differ from the previous tile's: P2 reloads them
                         const float rr = __shfl_sync(0xffffffffu, ref_lane, 2 * (lane & 15));
                         float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
@@ -979,8 +991,23 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     }
                     tmem_st8(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
                     tmem_wait_st();
+                    return true;
+                };
+                using T_ = std::true_type;
+                using F_ = std::false_type;
+                const bool have_ref = t0 < n_tiles;    // the group has a tile of this slab
+                for (int t = t0, j = 0; t < n_tiles; t += 2, ++j) {
+                    const bool full_tile = (t + 1) * kTileRows <= len;
+                    bool done;
+                    if (j == 0) done = full_tile ? p1_tile(T_{}, T_{}, t, j) : p1_tile(T_{}, F_{}, t, j);
+                    else done = full_tile ? p1_tile(F_{}, T_{}, t, j) : p1_tile(F_{}, F_{}, t, j);
+                    if (!done) {
+                        ok = false;
+                        break;
+                    }
                 }
                 if (!ok) break;
+                const float z_lane = warp_rows16<false>(zacc, true);   // row (lane >> 1)'s sum over the lanes
                 if ((lane & 1) == 0)
                     stats[((q * 2 + grp) * 4 + quad) * kRP + rh * 16 + (lane >> 1)] =
                         make_float2(have_ref ? ref_lane : -INFINITY, z_lane);

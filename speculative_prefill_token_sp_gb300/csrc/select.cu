@@ -466,15 +466,38 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
             __syncthreads();
         }
     }
+    // The chunk sums in ranked order, gathered by all threads into the sort's
+    // key array (no longer needed); the two running sums below stay serial
+    // (their fixed order is part of the definition) but read their operands
+    // sixteen at a time, ahead of the additions.
+    double* ranked = reinterpret_cast<double*>(keys);
+    for (int k = tid; k < nc; k += blockDim.x) ranked[k] = sums[c0 + idx[k]];
+    __syncthreads();
     if (tid == 0) {
         double total = 0.0;
-        for (int c = 0; c < nc; ++c) total = __dadd_rn(total, sums[c0 + c]);
+        int c = 0;
+        for (; c + 16 <= nc; c += 16) {
+            double v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = sums[c0 + c + k];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) total = __dadd_rn(total, v[k]);
+        }
+        for (; c < nc; ++c) total = __dadd_rn(total, sums[c0 + c]);
         const double target = __dmul_rn(g.rate, total);
         double cum = 0.0;
         int kstar = nc;
-        for (int k = 0; k < nc; ++k) {
-            cum = __dadd_rn(cum, sums[c0 + idx[k]]);
-            if (cum >= target) { kstar = k + 1; break; }
+        for (int k0 = 0; k0 < nc && kstar == nc; k0 += 16) {
+            double v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = k0 + k < nc ? ranked[k0 + k] : 0.0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if (k0 + k < nc && kstar == nc) {
+                    cum = __dadd_rn(cum, v[k]);
+                    if (cum >= target) kstar = k0 + k + 1;
+                }
+            }
         }
         s_kstar = kstar;
     }
