@@ -21,7 +21,8 @@
 // (3) one CTA per prompt: radix select of exactly kc chunks on (score desc,
 // index asc) with the keys in registers (prompts of up to 4096 chunks; longer
 // ones read them from memory each pass), or a bitonic sort of (mean desc,
-// index asc) and the running-mass cut; then the exclusive scan of kept chunk
+// index asc) and the running-mass cut (the total and the ranked running sums
+// in two warps side by side); then the exclusive scan of kept chunk
 // sizes and, for chunks of up to 256 tokens, the kept positions themselves;
 // (4) compaction of the kept positions for larger chunks or longer prompts;
 // (5) the guide's v2 keep rules (sp_select_rules).
@@ -70,10 +71,19 @@ __device__ __forceinline__ int find_batch(const int64_t* cu, int B, int64_t x) {
     return lo;
 }
 
+// Min-max normalisation of one prompt: x -> (x - mn) / (mx - mn), every score
+// 1.0 when mx == mn.  den = mx - mn (one rounding) and rcp = 1 / den (correctly
+// rounded) are computed once per prompt.
+struct NormCoef {
+    double mn, den, rcp;
+    int flat;
+};
+
 // (0) min and max importance of each prompt (one CTA per prompt).
 __global__ void __launch_bounds__(1024) minmax_kernel(const SelGeo g, const float* __restrict__ imp,
-                                                      float2* __restrict__ mm) {
+                                                      NormCoef* __restrict__ mm, int32_t* __restrict__ hdr) {
     const int b = blockIdx.x;
+    if (hdr != nullptr && b == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
     const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
     float mn = INFINITY, mx = -INFINITY;
     for (int64_t i = threadIdx.x; i < Mb; i += blockDim.x) {
@@ -96,20 +106,39 @@ __global__ void __launch_bounds__(1024) minmax_kernel(const SelGeo g, const floa
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
-        if (threadIdx.x == 0) mm[b] = make_float2(mn, mx);
+        if (threadIdx.x == 0) {
+            NormCoef c;
+            c.flat = mx > mn ? 0 : 1;
+            c.mn = (double)mn;
+            c.den = __dsub_rn((double)mx, (double)mn);
+            c.rcp = c.flat ? 0.0 : __drcp_rn(c.den);
+            mm[b] = c;
+        }
     }
 }
 
 // Token score: fp64 importance, optionally normalised and boosted.
+//
+// The normalising division (x - mn) / den is correctly rounded without a
+// divide instruction (fp64 division is slow on this GPU): with rcp = RN(1/den),
+// q0 = RN(num * rcp) is within one ulp of num / den, the residual
+// num - q0 * den is exact in one fma, and RN(q0 + residual * rcp) is then the
+// correctly rounded quotient (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990).  No step underflows here: num and den are differences of fp32 values.
 __device__ __forceinline__ double token_score(const SelGeo& g, float v, int64_t i, int64_t Mb,
-                                              float2 mm) {
+                                              const NormCoef& nc) {
     double x = (double)v;
     if (g.has_boost) {
         if (g.normalize) {
-            if (mm.y > mm.x)
-                x = __ddiv_rn(__dsub_rn(x, (double)mm.x), __dsub_rn((double)mm.y, (double)mm.x));
-            else
+            if (!nc.flat) {
+                const double num = __dsub_rn(x, nc.mn);
+                const double q0 = __dmul_rn(num, nc.rcp);
+                const double r = __fma_rn(-q0, nc.den, num);
+                x = __fma_rn(r, nc.rcp, q0);
+            } else {
                 x = 1.0;
+            }
         }
         if (i < (int64_t)g.first_n) x = __dmul_rn(x, g.first_mult);
         if (i >= Mb - (int64_t)g.last_n) x = __dmul_rn(x, g.last_mult);
@@ -121,12 +150,13 @@ __device__ __forceinline__ double token_score(const SelGeo& g, float v, int64_t 
 // Sum (left to right from 0.0) and mean (one divide) of global chunk gc;
 // sixteen loads in flight ahead of the additions.
 __device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __restrict__ imp,
-                                               const float2* __restrict__ mm, int64_t gc, double& sum, double& mean) {
+                                               const NormCoef* __restrict__ mm, int64_t gc, double& sum, double& mean) {
     const int b = find_batch(g.cn, g.B, gc);
     const int64_t c = gc - g.cn[b];
     const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
     const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
-    const float2 mmb = g.has_boost && g.normalize ? mm[b] : make_float2(0.f, 0.f);
+    NormCoef mmb = {0.0, 0.0, 0.0, 1};
+    if (g.has_boost && g.normalize) mmb = mm[b];
     double s = 0.0;
     int64_t i = lo;
     for (; i + 16 <= hi; i += 16) {
@@ -141,7 +171,7 @@ __device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __r
     mean = __ddiv_rn(s, (double)(hi - lo));
 }
 
-__global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const float2* __restrict__ mm,
+__global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const NormCoef* __restrict__ mm,
                              double* __restrict__ sums, double* __restrict__ means, int32_t* __restrict__ hdr) {
     // a fresh status for the call (the workspace header)
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
@@ -161,7 +191,7 @@ __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, cons
 constexpr int kPoolBlock = 64;
 constexpr int kMaxPoolHalo = 224;        // r at most: the window's means fit in 4 KB
 __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kernel(const SelGeo g, const float* __restrict__ imp,
-                                                                const float2* __restrict__ mm,
+                                                                const NormCoef* __restrict__ mm,
                                                                 double* __restrict__ sums, double* __restrict__ means,
                                                                 double* __restrict__ pooled,
                                                                 int32_t* __restrict__ hdr) {
@@ -349,6 +379,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
     __shared__ int s_remaining;
     __shared__ int s_kstar;
     __shared__ int s_done;
+    __shared__ double s_total;
+    __shared__ double s_block[64];
 
     const int b = blockIdx.x;
     const int64_t c0 = g.cn[b];
@@ -439,67 +471,102 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         return;
     }
 
-    // Cumulative-mass mode: bitonic sort of (key = descending mean, index).
+    // Cumulative-mass mode.  Warp 0 adds the total mass in chunk order while
+    // the other warps sort (key = descending mean, index) bitonically, gather
+    // the chunk sums in ranked order into the sort's key array and add the
+    // running mass in ranked order, keeping every prefix in place; the cut is
+    // then found in parallel.  Both running sums stay serial (their order is
+    // part of the definition); the total's operands are loaded by the lanes
+    // 32 at a time, one block ahead of the additions.
     int P = 1;
     while (P < nc) P <<= 1;
     uint64_t* keys = reinterpret_cast<uint64_t*>(dsm);
     int* idx = reinterpret_cast<int*>(dsm + sizeof(uint64_t) * P);
-    for (int i = tid; i < P; i += blockDim.x) {
-        if (i < nc) { keys[i] = ~order_key(means[c0 + i]); idx[i] = i; }
-        else        { keys[i] = ~0ull; idx[i] = 0x7fffffff; }
-    }
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < P / 2; i += blockDim.x) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const uint64_t ka = keys[lo], kb = keys[hi];
-                const int ia = idx[lo], ib = idx[hi];
-                const bool a_gt_b = ka > kb || (ka == kb && ia > ib);
-                if (a_gt_b == up) {
-                    keys[lo] = kb; keys[hi] = ka;
-                    idx[lo] = ib; idx[hi] = ia;
-                }
-            }
-            __syncthreads();
-        }
-    }
-    // The chunk sums in ranked order, gathered by all threads into the sort's
-    // key array (no longer needed); the two running sums below stay serial
-    // (their fixed order is part of the definition) but read their operands
-    // sixteen at a time, ahead of the additions.
     double* ranked = reinterpret_cast<double*>(keys);
-    for (int k = tid; k < nc; k += blockDim.x) ranked[k] = sums[c0 + idx[k]];
-    __syncthreads();
-    if (tid == 0) {
+    if (tid < 32) {
+        // blocks of 32 operands pass through a shared double buffer; every lane
+        // runs the same chain on broadcast reads
         double total = 0.0;
-        int c = 0;
-        for (; c + 16 <= nc; c += 16) {
-            double v[16];
+        double nxt = tid < nc ? sums[c0 + tid] : 0.0;
+        for (int base = 0, half = 0; base < nc; base += 32, half ^= 1) {
+            double* buf = s_block + 32 * half;
+            buf[tid] = nxt;
+            nxt = base + 32 + tid < nc ? sums[c0 + base + 32 + tid] : 0.0;
+            __syncwarp();
+            if (base + 32 <= nc) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = sums[c0 + c + k];
+                for (int h = 0; h < 2; ++h) {
+                    double v[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) total = __dadd_rn(total, v[k]);
-        }
-        for (; c < nc; ++c) total = __dadd_rn(total, sums[c0 + c]);
-        const double target = __dmul_rn(g.rate, total);
-        double cum = 0.0;
-        int kstar = nc;
-        for (int k0 = 0; k0 < nc && kstar == nc; k0 += 16) {
-            double v[16];
+                    for (int k = 0; k < 16; ++k) v[k] = buf[16 * h + k];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = k0 + k < nc ? ranked[k0 + k] : 0.0;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                if (k0 + k < nc && kstar == nc) {
-                    cum = __dadd_rn(cum, v[k]);
-                    if (cum >= target) kstar = k0 + k + 1;
+                    for (int k = 0; k < 16; ++k) total = __dadd_rn(total, v[k]);
                 }
+            } else {
+                for (int k = 0; k < nc - base; ++k) total = __dadd_rn(total, buf[k]);
             }
         }
-        s_kstar = kstar;
+        if (tid == 0) {
+            s_total = total;
+            s_kstar = nc;                          // every chunk, if the target is never reached
+        }
+    } else {
+        const int t = tid - 32, nt = (int)blockDim.x - 32;   // the sorting threads (named barrier 1)
+        for (int i = t; i < P; i += nt) {
+            if (i < nc) { keys[i] = ~order_key(means[c0 + i]); idx[i] = i; }
+            else        { keys[i] = ~0ull; idx[i] = 0x7fffffff; }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = t; i < P / 2; i += nt) {
+                    const int lo = 2 * i - (i & (stride - 1));
+                    const int hi = lo + stride;
+                    const bool up = (lo & size) == 0;
+                    const uint64_t ka = keys[lo], kb = keys[hi];
+                    const int ia = idx[lo], ib = idx[hi];
+                    const bool a_gt_b = ka > kb || (ka == kb && ia > ib);
+                    if (a_gt_b == up) {
+                        keys[lo] = kb; keys[hi] = ka;
+                        idx[lo] = ib; idx[hi] = ia;
+                    }
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
+            }
+        }
+        for (int k = t; k < nc; k += nt) ranked[k] = sums[c0 + idx[k]];
+        asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
+        if (t == 0) {
+            double cum = 0.0;
+            int k0 = 0;
+            for (; k0 + 16 <= nc; k0 += 16) {
+                double v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = ranked[k0 + k];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    cum = __dadd_rn(cum, v[k]);
+                    v[k] = cum;
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) ranked[k0 + k] = v[k];
+            }
+            for (; k0 < nc; ++k0) {
+                cum = __dadd_rn(cum, ranked[k0]);
+                ranked[k0] = cum;
+            }
+        }
+    }
+    __syncthreads();
+    {
+        // kstar = 1 + the first ranked position whose running mass reaches tau * total
+        const double target = __dmul_rn(g.rate, s_total);
+        for (int k = tid; k < nc; k += blockDim.x) {
+            if (ranked[k] >= target) {
+                atomicMin(&s_kstar, k + 1);
+                break;
+            }
+        }
     }
     __syncthreads();
     const int kstar = s_kstar;
@@ -637,7 +704,7 @@ SelLayout sel_layout(const SelectProblem& p) {
     Carve c;
     SelLayout lo;
     const size_t nc = (size_t)std::max<int64_t>(p.total_chunks, 1);
-    lo.mm = c.take(sizeof(float2) * std::max(p.B, 1));
+    lo.mm = c.take(sizeof(NormCoef) * std::max(p.B, 1));
     lo.sums = c.take(sizeof(double) * nc);
     lo.means = c.take(sizeof(double) * nc);
     lo.pooled = c.take(sizeof(double) * nc);
@@ -679,7 +746,7 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     g.cu[0] = p.cu_M_host[0];
     const SelLayout lo = sel_layout(p);
     char* w = static_cast<char*>(ws);
-    float2* mm = reinterpret_cast<float2*>(w + lo.mm);
+    NormCoef* mm = reinterpret_cast<NormCoef*>(w + lo.mm);
     double* sums = reinterpret_cast<double*>(w + lo.sums);
     double* means = reinterpret_cast<double*>(w + lo.means);
     double* pooled = reinterpret_cast<double*>(w + lo.pooled);
@@ -687,15 +754,17 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     int64_t* offs = reinterpret_cast<int64_t*>(w + lo.offs);
 
     const int64_t total = g.cn[p.B];
-    // the header is cleared by the chunk kernel (or here, when there are no chunks)
-    if (total == 0 || (p.has_boost && p.boost.normalize)) SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
-    if (p.has_boost && p.boost.normalize) {
-        minmax_kernel<<<p.B, 1024, 0, st>>>(g, p.importance, mm);
+    // the header is cleared by the min/max kernel or the chunk kernel (or here,
+    // when there are no chunks)
+    const bool normalize = p.has_boost && p.boost.normalize;
+    if (total == 0) SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
+    if (normalize && total > 0) {
+        minmax_kernel<<<p.B, 1024, 0, st>>>(g, p.importance, mm, static_cast<int32_t*>(ws));
         SP_LAUNCH_CHECK();
     }
     if (total > 0) {
         // small blocks: the fixed-order fp64 sums run on as many SMs as possible
-        int32_t* hdr = (p.has_boost && p.boost.normalize) ? nullptr : static_cast<int32_t*>(ws);
+        int32_t* hdr = normalize ? nullptr : static_cast<int32_t*>(ws);
         const bool pool = p.mode == SP_SELECT_TOPK && p.pool_k > 1;
         if (pool && (p.pool_k - 1) / 2 <= kMaxPoolHalo) {
             const int threads = (kPoolBlock + (p.pool_k - 1) + 31) / 32 * 32;     // 64 + 2r means, whole warps
