@@ -125,7 +125,7 @@ constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per wait
 std::atomic<unsigned long long> g_exchange_wait_ns{kTimeoutNs};
 
 struct TcParams {
-    int L, H, H_kv, G, N, R, d;
+    int L, H, H_kv, G, N, R, d;   // N: look-ahead steps of this pass (R = N * G query rows)
     int S;              // slabs = L * H_kv
     int P;              // CTAs
     int F;              // slab classes: CTA c takes slabs s = c % F, c % F + F, ...
@@ -160,7 +160,9 @@ struct TcParams {
     unsigned* acc_glob;             // [N][T] order-preserving codes of the combined maxima (F > 1)
     int* arrivals;                  // [Pc] CTAs of a range done with their maxima (F > 1)
     const __nv_bfloat16* Qp;        // the prompt's look-ahead queries [N, L, H, d] (preparation)
-    const __nv_bfloat16* Klap;      // its look-ahead keys [L, H_kv, N - la_shift, d] (preparation)
+    const __nv_bfloat16* Klap;      // its look-ahead keys [L, H_kv, N_total - la_shift, d] (preparation)
+    int N_total, j0;    // all steps of the call; this pass takes steps j0 .. j0 + N - 1
+    int accumulate;     // 1: add this pass's share of the mean to importance (passes after the first)
 };
 
 // Prompts of one batched launch ("wave"): prompt b owns CTAs [cta0[b], cta0[b+1])
@@ -522,14 +524,14 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     // eight consecutive lanes per row, one key each (keys k, k + 8, ... folded
     // in), every dot product from independent 16-byte loads
     if (!p.lse_mode) {
-        const int nk = p.N - p.la_shift;              // look-ahead keys stored per (layer, KV head)
+        const int nk = p.N_total - p.la_shift;        // look-ahead keys stored per (layer, KV head)
         const int sub = lane & 7;
         for (int r = warp * 4 + (lane >> 3); r < kRP; r += (blockDim.x / 32) * 4) {
             float m = -INFINITY, z = 0.f;
             if (r < p.R) {
-                const int j = r / p.G, h = g * p.G + r % p.G;
+                const int j = r / p.G, h = g * p.G + r % p.G;      // step j0 + j of the call
                 const uint4* q = reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d);
-                for (int k = sub; k <= j - p.la_shift; k += 8) {
+                for (int k = sub; k <= p.j0 + j - p.la_shift; k += 8) {
                     const uint4* kk = reinterpret_cast<const uint4*>(Kla + (((size_t)l * p.H_kv + g) * nk + k) * p.d);
                     // eight 16-byte chunks of both rows in flight at a time (d <= 128)
                     float u = 0.f;
@@ -586,7 +588,8 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
         if (threadIdx.x < kRP) {
             const int r = threadIdx.x;
             float v = 0.f;
-            if (r < p.R) v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N + r / p.G] * 1.4426950408889634f;
+            if (r < p.R)
+                v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N_total + p.j0 + r / p.G] * 1.4426950408889634f;
             lse[(size_t)s * kRP + r] = (unsigned long long)__float_as_uint(v) | (1ull << 32);
         }
     } else {
@@ -1069,7 +1072,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
         }
         epi_sync();                                    // both groups' running maxima are complete
         // importance of a token: (1/N) sum_j exp(max_{l,h}(s - lse))
-        const float inv_n = 1.0f / (float)p.N;
+        const float inv_n = 1.0f / (float)p.N_total;
         const size_t half = (size_t)p.n_tiles_max * p.N * kTileRows;
         if (p.F == 1) {
             if (!*abort_flag && rh == 0) {
@@ -1079,7 +1082,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                         const float* a = acc + (size_t)t * p.N * kTileRows + tok;
                         float sum = 0.f;
                         for (int jj = 0; jj < p.N; ++jj) sum += exp2f(fmaxf(a[jj * kTileRows], a[half + jj * kTileRows]));
-                        p.importance[t_begin + k] = sum * inv_n;
+                        p.importance[t_begin + k] = (p.accumulate ? p.importance[t_begin + k] : 0.f) + sum * inv_n;
                     }
                 }
             }
@@ -1110,7 +1113,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                         float sum = 0.f;
                         for (int jj = 0; jj < p.N; ++jj)
                             sum += exp2f(order_decode(__ldcg(&p.acc_glob[(size_t)jj * p.T + t_begin + k])));
-                        p.importance[t_begin + k] = sum * inv_n;
+                        p.importance[t_begin + k] = (p.accumulate ? p.importance[t_begin + k] : 0.f) + sum * inv_n;
                     }
                 }
             }
@@ -1290,12 +1293,20 @@ int sm_count_or(int fallback) {
     return n;
 }
 
+// Look-ahead steps j0 .. j0 + n - 1 of a call: the query rows of one kernel
+// pass.  A call with more than kRP / G steps runs in several passes (each
+// streams K once); later passes add their share of the mean to importance.
+struct Pass {
+    int j0, n;
+};
+
+int steps_per_pass(const ScoreProblem& q) { return kRP / (q.H / q.H_kv); }
+
 bool shape_ok(const ScoreProblem& q) {
     if (q.dtype != SP_BF16 || q.B < 1 || q.N < 1 || q.max_M < 1) return false;
     if (q.d != 64 && q.d != 128) return false;
     const int G = q.H / q.H_kv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return false;
-    if (q.N * G > kRP) return false;
     if (q.T < 1 || q.T > (int64_t)INT32_MAX / 4) return false;
     if ((int64_t)q.L * q.H_kv * q.T > (int64_t)INT32_MAX) return false;   // TMA row coordinate
     return true;
@@ -1303,10 +1314,14 @@ bool shape_ok(const ScoreProblem& q) {
 
 // Plan for one prompt of M tokens of the problem's shape on up to P_hint CTAs;
 // returns false if it does not fit this path.
-bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Plan& out) {
+bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Pass ps, Plan& out) {
     if (!shape_ok(q) || M < 1 || M > q.max_M) return false;
+    if (ps.n < 1 || ps.j0 < 0 || ps.j0 + ps.n > q.N || ps.n * (q.H / q.H_kv) > kRP) return false;
     TcParams& p = out.p;
-    p.L = q.L; p.H = q.H; p.H_kv = q.H_kv; p.G = q.H / q.H_kv; p.N = q.N; p.R = q.N * p.G; p.d = q.d;
+    p.L = q.L; p.H = q.H; p.H_kv = q.H_kv; p.G = q.H / q.H_kv; p.N = ps.n; p.R = ps.n * p.G; p.d = q.d;
+    p.N_total = q.N;
+    p.j0 = ps.j0;
+    p.accumulate = ps.j0 > 0 ? 1 : 0;
     p.S = q.L * q.H_kv;
     p.T = M;
     p.slab_stride = q.T;
@@ -1477,7 +1492,7 @@ void bind_prompt(const ScoreProblem& q, int b, bool first, uint8_t* ws, uint8_t*
     p.importance = q.importance + q.cu_M_host[b];
     p.acc_glob = reinterpret_cast<unsigned*>(w + plan.off_acc_glob);
     p.arrivals = reinterpret_cast<int*>(w + plan.off_arrivals);
-    p.Qp = static_cast<const __nv_bfloat16*>(q.Q) + (size_t)b * q.N * q.L * q.H * q.d;
+    p.Qp = static_cast<const __nv_bfloat16*>(q.Q) + ((size_t)b * q.N + p.j0) * q.L * q.H * q.d;
     p.Klap = q.Kla ? static_cast<const __nv_bfloat16*>(q.Kla) + (size_t)b * q.L * q.H_kv * (q.N - q.la_shift) * q.d
                    : nullptr;
     p.lse_in = q.lse_in ? q.lse_in + (size_t)b * q.L * q.H * q.N : nullptr;   // [B, L, H, N]
@@ -1495,7 +1510,7 @@ struct Wave {
     int smem = 0;               // the largest plan's shared memory
 };
 
-bool plan_waves(const ScoreProblem& q, int sms, std::vector<Wave>& waves) {
+bool plan_waves(const ScoreProblem& q, int sms, Pass ps, std::vector<Wave>& waves) {
     waves.clear();
     const int64_t per_cta = (int64_t)kMaxTiles * kTileRows;      // tokens of a slab one CTA can take
     auto len = [&](int b) { return q.cu_M_host[b + 1] - q.cu_M_host[b]; };
@@ -1519,7 +1534,7 @@ bool plan_waves(const ScoreProblem& q, int sms, std::vector<Wave>& waves) {
         size_t off = 0;
         for (int i = 0; i < n; ++i) {
             Plan plan;
-            if (!make_plan(q, len(cur[i]), P[i], plan)) return false;
+            if (!make_plan(q, len(cur[i]), P[i], ps, plan)) return false;
             w.plans.push_back(plan);
             w.offs.push_back(off);
             off += align_up(plan.total);
@@ -1553,29 +1568,34 @@ unsigned long long score_tc_set_exchange_wait_ns(unsigned long long ns) {
     return g_exchange_wait_ns.exchange(ns == 0 ? kTimeoutNs : ns);
 }
 
+// The first pass has the most steps (the largest workspace).
+Pass first_pass(const ScoreProblem& q) { return Pass{0, std::min(q.N, steps_per_pass(q))}; }
+
 bool score_tc_supported(const ScoreProblem& q) {
     Plan plan;
-    return make_plan(q, q.max_M, sm_count_or(148), plan);
+    return shape_ok(q) && make_plan(q, q.max_M, sm_count_or(148), first_pass(q), plan);
 }
 
 size_t score_tc_ws_bytes(const ScoreProblem& q) {
-    // prompt after prompt, the workspace is reused: the largest prompt needs the most
+    // prompt after prompt (and pass after pass) the workspace is reused: the
+    // largest prompt of the first pass needs the most
+    if (!shape_ok(q)) return 0;
     Plan plan;
-    size_t bytes = make_plan(q, q.max_M, kMaxCtas, plan) ? plan.total : 0;
+    size_t bytes = make_plan(q, q.max_M, kMaxCtas, first_pass(q), plan) ? plan.total : 0;
     if (bytes > 0 && use_waves(q)) {
         std::vector<Wave> waves;
-        if (plan_waves(q, sm_count_or(148), waves))
+        if (plan_waves(q, sm_count_or(148), first_pass(q), waves))
             for (const Wave& w : waves) bytes = std::max(bytes, w.bytes);
     }
     return bytes;
 }
 
 // One prompt (b) of a packed batch: its plan, workspace pointers and launches.
-static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const KMaps& maps, int sms,
+static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const KMaps& maps, int sms, Pass ps,
                                void* ws, cudaStream_t st) {
     const int64_t M = q.cu_M_host[b + 1] - q.cu_M_host[b];
     Plan plan;
-    if (!make_plan(q, M, sms, plan)) {
+    if (!make_plan(q, M, sms, ps, plan)) {
         set_error("sp_score: prompt %d (%lld tokens) is outside the tensor-core path", b, (long long)M);
         return SP_EUNSUPPORTED;
     }
@@ -1660,30 +1680,38 @@ sp_status score_tc_launch(const ScoreProblem& q, void* ws, cudaStream_t st) {
         }
     }
 
-    // a batch: wave after wave, each wave's prompts side by side on the SMs
-    // (stream order separates the waves, which reuse the workspace)
-    std::vector<Wave> waves;
-    if (use_waves(q) && plan_waves(q, sms, waves)) {
-        size_t need = 0;
-        for (const Wave& w : waves) need = std::max(need, w.bytes);
-        if (need <= score_tc_ws_bytes(q)) {
-            bool first = true;
-            for (Wave& w : waves) {
-                const sp_status s = launch_wave(q, w, first, maps, ws, st);
-                if (s != SP_OK) return s;
-                first = false;
-            }
-            return SP_OK;
-        }
-    }
-    // otherwise one prompt after another, each with its own plan over all SMs;
-    // they share the workspace (stream order separates them)
+    // Pass after pass (steps j0 .. j0 + n - 1 each, stream-ordered, sharing
+    // the workspace); the first launch of the call clears the status.
+    const size_t ws_cap = score_tc_ws_bytes(q);
+    const int per = steps_per_pass(q);
     bool first = true;
-    for (int b = 0; b < q.B; ++b) {
-        if (q.cu_M_host[b + 1] == q.cu_M_host[b]) continue;
-        const sp_status s = launch_prompt(q, b, first, maps, sms, ws, st);
-        if (s != SP_OK) return s;
-        first = false;
+    for (int j0 = 0; j0 < q.N; j0 += per) {
+        const Pass ps{j0, std::min(per, q.N - j0)};
+        // a batch: wave after wave, each wave's prompts side by side on the SMs
+        // (stream order separates the waves, which reuse the workspace)
+        std::vector<Wave> waves;
+        bool done = false;
+        if (use_waves(q) && plan_waves(q, sms, ps, waves)) {
+            size_t need = 0;
+            for (const Wave& w : waves) need = std::max(need, w.bytes);
+            if (need <= ws_cap) {
+                for (Wave& w : waves) {
+                    const sp_status s = launch_wave(q, w, first, maps, ws, st);
+                    if (s != SP_OK) return s;
+                    first = false;
+                }
+                done = true;
+            }
+        }
+        if (done) continue;
+        // otherwise one prompt after another, each with its own plan over all
+        // SMs; they share the workspace (stream order separates them)
+        for (int b = 0; b < q.B; ++b) {
+            if (q.cu_M_host[b + 1] == q.cu_M_host[b]) continue;
+            const sp_status s = launch_prompt(q, b, first, maps, sms, ps, ws, st);
+            if (s != SP_OK) return s;
+            first = false;
+        }
     }
     return SP_OK;
 }

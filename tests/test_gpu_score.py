@@ -75,6 +75,11 @@ SHAPES = [
     (1, 32, 4, 128, 4097, 8, "bf16"),
     (2, 4, 4, 8, 77, 16, "f32"),
     (1, 64, 1, 64, 200, 4, "bf16"),
+    # more query rows than one tensor-core pass takes (N * G > 32): passes of 32 / G steps
+    (2, 32, 8, 128, 3000, 16, "bf16"),       # two passes of 8 steps
+    (1, 16, 2, 64, 1500, 12, "bf16"),        # three passes of 4 steps
+    (2, 8, 8, 64, 700, 48, "bf16"),          # G = 1: passes of 32 and 16 steps
+    (1, 8, 4, 128, 5000, 30, "bf16"),        # G = 2: passes of 16 and 14 steps
 ]
 
 
@@ -98,6 +103,37 @@ def test_long_prompts_few_layers(sp, M):
     x = W.make_inputs(wl, seed=M)
     got = run_score(sp, x)
     check_importance(got, oracle.importance(x.Q_la, x.K_prompt, x.K_la), "bf16", f"M={M}")
+
+
+def test_more_steps_than_one_pass_runs_on_tensor_cores(sp):
+    """N = 16 look-ahead steps at the 8B head shape (64 query rows per KV head):
+    two tensor-core passes of 8 steps, each one preparation and one scoring
+    launch (the general path would launch 4 kernels once)."""
+    import torch
+    wl = W.Workload("t", L=2, H=32, H_kv=8, d=128, M=9000, N=16, dtype="bf16", chunk=32, pool_k=3, mode="topk",
+                    keep_rate=0.1, needle_frac=0.02, run_min=16, run_max=128)
+    x = W.make_inputs(wl, seed=16)
+    Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
+    n0 = sp.sp_kernel_launches()
+    imp = sp.score(Q, K, Kla, check=True)
+    torch.cuda.synchronize()
+    assert sp.sp_kernel_launches() - n0 == 4
+    check_importance(imp.cpu().numpy(), oracle.importance(x.Q_la, x.K_prompt, x.K_la), "bf16", "N=16")
+
+
+def test_varlen_more_steps_than_one_pass(sp):
+    """A ragged batch with N * G = 48 rows: every wave runs twice (steps 0-7, 8-11)."""
+    import torch
+    wl = W.Workload("t", L=2, H=16, H_kv=4, d=64, M=0, N=12, dtype="bf16", chunk=32, pool_k=1, mode="mass",
+                    mass=0.85, needle_frac=0.05, run_min=8, run_max=64)
+    v = W.make_varlen_inputs(wl, 48, lengths=[3000, 0, 700, 5000, 64])
+    Q, K, Kla, cu = v.packed()
+    got = sp.score_varlen(to_device(Q), to_device(K), to_device(Kla), cu, check=True)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    for b, r in enumerate(v.requests):
+        if r.M:
+            check_importance(got[cu[b]:cu[b + 1]], oracle.importance(r.Q_la, r.K_prompt, r.K_la), "bf16", f"req {b}")
 
 
 def test_varlen_ragged_with_empty_prompts(sp):

@@ -57,6 +57,8 @@ SHAPES = [
     (3, 8, 8, 64, 300, 1, "bf16"),
     (1, 32, 4, 128, 4097, 8, "bf16"),
     (2, 6, 3, 72, 513, 5, "bf16"),         # general path (d = 72)
+    (2, 32, 8, 128, 2500, 16, "bf16"),     # two tensor-core passes of 8 steps
+    (1, 16, 2, 64, 900, 10, "bf16"),       # passes of 4, 4 and 2 steps
     (1, 16, 2, 256, 257, 4, "f32"),
 ]
 

@@ -27,6 +27,7 @@ SHAPES = [
     (2, 32, 8, 128, 8192, 7, "bf16"),      # 8 rows x G 4 = 32: tensor cores
     (1, 32, 8, 128, 40960, 7, "bf16"),
     (2, 4, 2, 64, 300, 0, "bf16"),         # only the prefill row
+    (2, 32, 8, 128, 3000, 11, "bf16"),     # 12 rows: passes of 8 and 4 steps (the second sees keys 0..10)
     (2, 4, 2, 64, 513, 3, "f32"),          # general path
 ]
 
