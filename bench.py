@@ -54,6 +54,9 @@ def parse_args(argv=None):
                     help="skip the other workloads' timings (8K, 128K, the v3 batch, tiny)")
     ap.add_argument("--bare", action="store_true",
                     help="run only the warm-up and timed steps and print their time (for profilers)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="with --bare: the first LAYERS layers of the workload only (a smaller case of the same "
+                         "per-slab plan, for ncu captures)")
     return ap.parse_args(argv)
 
 
@@ -431,6 +434,11 @@ def run_gpu(args) -> None:
     wl = W.BY_NAME[args.workload]
     assert wl.batch == 1, "bench runs a single-prompt workload"
     x = W.make_inputs(wl, wl.seed)
+    if args.layers:
+        assert args.bare and 0 < args.layers <= wl.L, "--layers takes --bare and at most the workload's layers"
+        import dataclasses
+        wl = dataclasses.replace(wl, L=args.layers)
+        x = dataclasses.replace(_slice_layers(x, 0, args.layers), wl=wl)
 
     Q, K, Kla = upload(x.Q_la, dev), upload(x.K_prompt, dev), upload(x.K_la, dev)
     dt = sp.SP_BF16 if wl.dtype == "bf16" else sp.SP_F32
@@ -476,7 +484,7 @@ def run_gpu(args) -> None:
         e1.record(stream)
         torch.cuda.synchronize()
         if rank == 0:
-            print(json.dumps({"bare": True, "workload": wl.name, "steps": args.steps,
+            print(json.dumps({"bare": True, "workload": wl.name, "layers": wl.L, "steps": args.steps,
                               "ms_per_step": e0.elapsed_time(e1) / args.steps}), flush=True)
         return
 
