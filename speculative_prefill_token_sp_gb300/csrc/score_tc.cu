@@ -533,20 +533,18 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
                 const uint4* q = reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d);
                 for (int k = sub; k <= p.j0 + j - p.la_shift; k += 8) {
                     const uint4* kk = reinterpret_cast<const uint4*>(Kla + (((size_t)l * p.H_kv + g) * nk + k) * p.d);
-                    // eight 16-byte chunks of both rows in flight at a time (d <= 128)
+                    // four 16-byte chunks of both rows in flight at a time
                     float u = 0.f;
-                    for (int c0 = 0; c0 < p.d / 8; c0 += 8) {
-                        uint4 a[8], b[8];
+                    for (int c0 = 0; c0 < p.d / 8; c0 += 4) {
+                        uint4 a[4], b[4];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            if (c0 + c < p.d / 8) {
-                                a[c] = q[c0 + c];
-                                b[c] = kk[c0 + c];
-                            }
+                        for (int c = 0; c < 4; ++c) {
+                            a[c] = q[c0 + c];
+                            b[c] = kk[c0 + c];
                         }
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            if (c0 + c < p.d / 8) {
+                        for (int c = 0; c < 4; ++c) {
+                            {
                                 const uint32_t aw[4] = {a[c].x, a[c].y, a[c].z, a[c].w};
                                 const uint32_t bw[4] = {b[c].x, b[c].y, b[c].z, b[c].w};
 #pragma unroll
@@ -607,13 +605,14 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     }
 }
 
-// (two blocks per SM: a call's 256 or so slabs then run in one wave)
-__global__ void __launch_bounds__(256, 2) tc_prep_kernel(const __grid_constant__ TcParams p) {
+// (four blocks per SM: a call's 256 or so slabs, or a wave's several hundred,
+// run in one or two rounds)
+__global__ void __launch_bounds__(256, 4) tc_prep_kernel(const __grid_constant__ TcParams p) {
     tc_prep_body(p, blockIdx.x);
 }
 
 // All prompts of a wave: blocks b * S .. b * S + S - 1 prepare prompt b.
-__global__ void __launch_bounds__(256, 2) tc_prep_batch_kernel(const __grid_constant__ TcBatch bt) {
+__global__ void __launch_bounds__(256, 4) tc_prep_batch_kernel(const __grid_constant__ TcBatch bt) {
     const int S = bt.p[0].S;
     tc_prep_body(bt.p[blockIdx.x / S], blockIdx.x % S);
 }
@@ -940,6 +939,15 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                     if (++ls == p.land) { ls = 0; lph ^= 1; }
                     const bool valid = kFull || t * kTileRows + tok < len;
                     float o[16];
+                    uint32_t pk[8];
+                    auto pack_store = [&]() {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const __half2 h2 = __floats2half2_rn(o[2 * k], o[2 * k + 1]);
+                            pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        tmem_st8(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
+                    };
                     bool redo = true;
                     if constexpr (kFirst) {
 #pragma unroll
@@ -952,6 +960,9 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                         const float m4 = fmax3(o[12], o[13], o[14]);
                         const float om = fmaxf(fmax3(m0, m1, m2), fmax3(m3, m4, o[15]));
                         redo = __any_sync(0xffffffffu, (kFull || valid) && om > kRefMargin);
+                        // the fp16 offsets with the current references go to TMEM
+                        // while the vote resolves (stored again if a reference rises)
+                        pack_store();
                     }
                     if (redo) {
                         // each reference starts at its row's largest value (first
@@ -973,12 +984,13 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                         }
                         if ((lane & 1) == 0) wref[lane >> 1] = ref_lane;
                         __syncwarp();
-                    }
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const __half2 h2 = __floats2half2_rn(o[2 * k], o[2 * k + 1]);
-                        pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+                        // the tile's fp16 references differ from the previous tile's: P2 reloads them
+                        const float rr = __shfl_sync(0xffffffffu, ref_lane, 2 * (lane & 15));
+                        float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
+                        if (lane < 16) cq[lane] = rr;
+                        chg |= 1u << (hs * tpg + j);
+                        if constexpr (!kFirst) tmem_wait_st();   // the first store has landed before this one
+                        pack_store();
                     }
                     if constexpr (kFull) {
 #pragma unroll
@@ -988,14 +1000,6 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
 #pragma unroll
                         for (int r = 0; r < 16; ++r) zacc[r] += valid ? ex2_approx(o[r]) : 0.f;
                     }
-                    if (redo) {
-                        // the tile's fp16 references differ from the previous tile's: P2 reloads them
-                        const float rr = __shfl_sync(0xffffffffu, ref_lane, 2 * (lane & 15));
-                        float* cq = cb_g + (((size_t)hs * tpg + j) * 4 + quad) * kRP + rh * 16;
-                        if (lane < 16) cq[lane] = rr;
-                        chg |= 1u << (hs * tpg + j);
-                    }
-                    tmem_st8(held_g + (uint32_t)((hs * tpg + j) * 16), pk);
                     tmem_wait_st();
                     return true;
                 };
