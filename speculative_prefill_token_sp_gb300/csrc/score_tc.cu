@@ -101,7 +101,13 @@ constexpr int kBoxRows = 32;         // rows per TMA box of a slab's ragged last
 constexpr int kUnit = 32;            // token-range granularity
 constexpr int kRP = 32;              // query rows per slab, padded (MMA N)
 constexpr int kMaxCtas = 256;
-constexpr int kMaxTiles = 8;         // tiles per CTA per slab
+constexpr int kMaxTiles = 8;         // tiles per CTA per slab for slab classes and batch waves
+// Tiles per CTA per slab that a plan may have at most: prompts longer than
+// kMaxTiles tiles on every CTA (about 155K tokens at 152 CTAs) keep the
+// tensor-core path with fewer held slabs (down to none: P2 right after P1),
+// as far as the running maxima leave shared memory for two K stages (about
+// 270K tokens at the 8B shape, 310K at d = 64)
+constexpr int kMaxTilesLong = 16;
 // How far (base-2 units) a logit may rise above its row's reference before the
 // epilogue retakes the reference (3 = 2.08 in natural-log units): fp16 offsets
 // below it keep the dominant values of a row to about 2^-11 relative.
@@ -1349,7 +1355,7 @@ bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Pass ps, Plan& out)
     p.P = p.Pc * p.F;
     const int units_max = (p.U + p.Pc - 1) / p.Pc;
     p.n_tiles_max = (units_max * kUnit + kTileRows - 1) / kTileRows;
-    if (p.n_tiles_max > kMaxTiles) return false;
+    if (p.n_tiles_max > kMaxTilesLong) return false;
     // TMEM: per epilogue group `land` fp32 landing tiles (32 columns each) and
     // `held` slabs of its fp16 tiles (16 columns per tile, tiles_per_group tiles
     // per slab); two landing tiles when that still leaves room for two held slabs.

@@ -94,14 +94,18 @@ def test_random_shapes(sp, shape):
     check_importance(got, ref, dt, str(shape))
 
 
-@pytest.mark.parametrize("M", [40960, 65536, 98305, 131072])
+@pytest.mark.parametrize("M", [40960, 65536, 98305, 131072, 200000, 270000])
 def test_long_prompts_few_layers(sp, M):
-    """3 to 7 tiles of 128 tokens per CTA per slab and short look-behind (lag)
-    windows, on one layer of the 8B shape so that the oracle stays cheap."""
+    """3 to 14 tiles of 128 tokens per CTA per slab and short look-behind (lag)
+    windows (one held slab beyond about 155K tokens), on one layer of the 8B
+    shape so that the oracle stays cheap; every length stays on the
+    tensor-core path (one preparation and one scoring launch)."""
     wl = W.Workload("t", L=1, H=32, H_kv=8, d=128, M=M, N=8, dtype="bf16", chunk=64, pool_k=3, mode="topk",
                     keep_rate=0.1, needle_frac=0.01, run_min=16, run_max=128)
     x = W.make_inputs(wl, seed=M)
+    n0 = sp.sp_kernel_launches()
     got = run_score(sp, x)
+    assert sp.sp_kernel_launches() - n0 == 2
     check_importance(got, oracle.importance(x.Q_la, x.K_prompt, x.K_la), "bf16", f"M={M}")
 
 
