@@ -169,6 +169,8 @@ struct TcParams {
     const __nv_bfloat16* Klap;      // its look-ahead keys [L, H_kv, N_total - la_shift, d] (preparation)
     int N_total, j0;    // all steps of the call; this pass takes steps j0 .. j0 + N - 1
     int accumulate;     // 1: add this pass's share of the mean to importance (passes after the first)
+    int Gr;             // query heads per KV head; G (>= Gr, a power of two) query rows per step, the
+                        // rows past Gr of each step are zero padding that P2 leaves out
 };
 
 // Prompts of one batched launch ("wave"): prompt b owns CTAs [cta0[b], cta0[b+1])
@@ -474,6 +476,15 @@ __device__ __forceinline__ float fold_heads(float m, const float* y) {
     return m;
 }
 
+// m = max(m, y[0], ..., y[gr-1]) for the first gr of G values (the rest are padding rows)
+template <int G>
+__device__ __forceinline__ float fold_heads_masked(float m, const float* y, int gr) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+        if (hh < gr) m = fmaxf(m, y[hh]);
+    return m;
+}
+
 // Order-preserving 32-bit code of a float (a < b  <=>  code(a) < code(b) as
 // unsigned), so that atomicMax on codes takes the max of floats; 0 is below
 // the code of every float.
@@ -521,8 +532,8 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     for (int u = 0; u < 2; ++u) {
         const int idx = threadIdx.x + u * (int)blockDim.x, r = idx / cpr, ch = idx % cpr;
         iv[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < kRP * cpr && r < p.R) {
-            const int j = r / p.G, h = g * p.G + r % p.G;
+        if (idx < kRP * cpr && r < p.R && r % p.G < p.Gr) {
+            const int j = r / p.G, h = g * p.Gr + r % p.G;
             iv[u] = *reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d + ch * 8);
         }
     }
@@ -534,8 +545,8 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
         const int sub = lane & 7;
         for (int r = warp * 4 + (lane >> 3); r < kRP; r += (blockDim.x / 32) * 4) {
             float m = -INFINITY, z = 0.f;
-            if (r < p.R) {
-                const int j = r / p.G, h = g * p.G + r % p.G;      // step j0 + j of the call
+            if (r < p.R && r % p.G < p.Gr) {
+                const int j = r / p.G, h = g * p.Gr + r % p.G;      // step j0 + j of the call
                 const uint4* q = reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d);
                 for (int k = sub; k <= p.j0 + j - p.la_shift; k += 8) {
                     const uint4* kk = reinterpret_cast<const uint4*>(Kla + (((size_t)l * p.H_kv + g) * nk + k) * p.d);
@@ -592,8 +603,9 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
         if (threadIdx.x < kRP) {
             const int r = threadIdx.x;
             float v = 0.f;
-            if (r < p.R)
-                v = p.lse_in[((size_t)l * p.H + g * p.G + r % p.G) * p.N_total + p.j0 + r / p.G] * 1.4426950408889634f;
+            if (r < p.R && r % p.G < p.Gr)
+                v = p.lse_in[((size_t)l * p.H + g * p.Gr + r % p.G) * p.N_total + p.j0 + r / p.G] *
+                    1.4426950408889634f;
             lse[(size_t)s * kRP + r] = (unsigned long long)__float_as_uint(v) | (1ull << 32);
         }
     } else {
@@ -850,7 +862,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
         float* wref = rbuf + ew * 16;                  // the warp's 16 row references (P1)
         const uint32_t held_g = tmem_base + lane_addr + (uint32_t)(p.held_base + grp * p.held * tpg * 16 + rh * 8);
         const int odd = n_tiles & 1;
-        const bool all_rows = p.R == kRP;              // every query row is a real (step, head) row
+        const bool all_rows = p.R == kRP && p.Gr == G;  // every query row is a real (step, head) row
         int ls = 0, lph = 0;                           // next landing tile of the group's ring, its phase
         int hs1 = 0, hs2 = 0;                          // held slots of the next P1 and P2 slabs
         uint32_t chg = 0;                              // held tiles (hs * tpg + j) whose references P2 reloads
@@ -889,7 +901,8 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
                             float y[G];
 #pragma unroll
                             for (int hh = 0; hh < G; ++hh) y[hh] = fmaf(x[jl * G + hh], p.scale_log2e, -lr[jl * G + hh]);
-                            a[jj * kTileRows] = fold_heads<G>(a[jj * kTileRows], y);
+                            a[jj * kTileRows] = p.Gr == G ? fold_heads<G>(a[jj * kTileRows], y)
+                                                          : fold_heads_masked<G>(a[jj * kTileRows], y, p.Gr);
                         }
                     }
                 }
@@ -1075,7 +1088,7 @@ __device__ __forceinline__ void tc_score_body(const KMaps& kmaps, const TcParams
 #pragma unroll
                         for (int jl = 0; jl < 16 / G; ++jl) {
                             const int jj = rh * (16 / G) + jl;
-                            if (jj < p.N) a[jj * kTileRows] = fold_heads<G>(av[jl], y + jl * G);
+                            if (jj < p.N) a[jj * kTileRows] = fold_heads_masked<G>(av[jl], y + jl * G, p.Gr);
                         }
                     }
                 }
@@ -1313,13 +1326,21 @@ struct Pass {
     int j0, n;
 };
 
-int steps_per_pass(const ScoreProblem& q) { return kRP / (q.H / q.H_kv); }
+// Query rows per look-ahead step: the heads of a KV group, padded to a power
+// of two (1, 2, 4, 8 or 16) so that a 16-row half of the MMA columns holds
+// whole steps.
+int padded_group(int G) {
+    int Gp = 1;
+    while (Gp < G) Gp <<= 1;
+    return Gp;
+}
+
+int steps_per_pass(const ScoreProblem& q) { return kRP / padded_group(q.H / q.H_kv); }
 
 bool shape_ok(const ScoreProblem& q) {
     if (q.dtype != SP_BF16 || q.B < 1 || q.N < 1 || q.max_M < 1) return false;
     if (q.d != 64 && q.d != 128) return false;
-    const int G = q.H / q.H_kv;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+    if (q.H / q.H_kv > 16) return false;
     if (q.T < 1 || q.T > (int64_t)INT32_MAX / 4) return false;
     if ((int64_t)q.L * q.H_kv * q.T > (int64_t)INT32_MAX) return false;   // TMA row coordinate
     return true;
@@ -1329,9 +1350,11 @@ bool shape_ok(const ScoreProblem& q) {
 // returns false if it does not fit this path.
 bool make_plan(const ScoreProblem& q, int64_t M, int P_hint, Pass ps, Plan& out) {
     if (!shape_ok(q) || M < 1 || M > q.max_M) return false;
-    if (ps.n < 1 || ps.j0 < 0 || ps.j0 + ps.n > q.N || ps.n * (q.H / q.H_kv) > kRP) return false;
+    const int Gp = padded_group(q.H / q.H_kv);
+    if (ps.n < 1 || ps.j0 < 0 || ps.j0 + ps.n > q.N || ps.n * Gp > kRP) return false;
     TcParams& p = out.p;
-    p.L = q.L; p.H = q.H; p.H_kv = q.H_kv; p.G = q.H / q.H_kv; p.N = ps.n; p.R = ps.n * p.G; p.d = q.d;
+    p.L = q.L; p.H = q.H; p.H_kv = q.H_kv; p.G = Gp; p.N = ps.n; p.R = ps.n * Gp; p.d = q.d;
+    p.Gr = q.H / q.H_kv;
     p.N_total = q.N;
     p.j0 = ps.j0;
     p.accumulate = ps.j0 > 0 ? 1 : 0;
@@ -1617,15 +1640,17 @@ static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const K
     const TcParams& p = plan.p;
     tc_prep_kernel<<<p.S, 256, 0, st>>>(p);
     SP_LAUNCH_CHECK();
-    switch (q.d * 16 + p.G) {
-        case 64 * 16 + 1: return launch_kernel<64, 1>(maps, p, st);
-        case 64 * 16 + 2: return launch_kernel<64, 2>(maps, p, st);
-        case 64 * 16 + 4: return launch_kernel<64, 4>(maps, p, st);
-        case 64 * 16 + 8: return launch_kernel<64, 8>(maps, p, st);
-        case 128 * 16 + 1: return launch_kernel<128, 1>(maps, p, st);
-        case 128 * 16 + 2: return launch_kernel<128, 2>(maps, p, st);
-        case 128 * 16 + 4: return launch_kernel<128, 4>(maps, p, st);
-        case 128 * 16 + 8: return launch_kernel<128, 8>(maps, p, st);
+    switch (q.d * 32 + p.G) {
+        case 64 * 32 + 1: return launch_kernel<64, 1>(maps, p, st);
+        case 64 * 32 + 2: return launch_kernel<64, 2>(maps, p, st);
+        case 64 * 32 + 4: return launch_kernel<64, 4>(maps, p, st);
+        case 64 * 32 + 8: return launch_kernel<64, 8>(maps, p, st);
+        case 64 * 32 + 16: return launch_kernel<64, 16>(maps, p, st);
+        case 128 * 32 + 1: return launch_kernel<128, 1>(maps, p, st);
+        case 128 * 32 + 2: return launch_kernel<128, 2>(maps, p, st);
+        case 128 * 32 + 4: return launch_kernel<128, 4>(maps, p, st);
+        case 128 * 32 + 8: return launch_kernel<128, 8>(maps, p, st);
+        case 128 * 32 + 16: return launch_kernel<128, 16>(maps, p, st);
         default: break;
     }
     set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, p.G);
@@ -1648,15 +1673,17 @@ static sp_status launch_wave(const ScoreProblem& q, Wave& wv, bool first, const 
     }
     tc_prep_batch_kernel<<<bt.nb * bt.p[0].S, 256, 0, st>>>(bt);
     SP_LAUNCH_CHECK();
-    switch (q.d * 16 + bt.p[0].G) {
-        case 64 * 16 + 1: return launch_batch<64, 1>(maps, bt, wv.smem, st);
-        case 64 * 16 + 2: return launch_batch<64, 2>(maps, bt, wv.smem, st);
-        case 64 * 16 + 4: return launch_batch<64, 4>(maps, bt, wv.smem, st);
-        case 64 * 16 + 8: return launch_batch<64, 8>(maps, bt, wv.smem, st);
-        case 128 * 16 + 1: return launch_batch<128, 1>(maps, bt, wv.smem, st);
-        case 128 * 16 + 2: return launch_batch<128, 2>(maps, bt, wv.smem, st);
-        case 128 * 16 + 4: return launch_batch<128, 4>(maps, bt, wv.smem, st);
-        case 128 * 16 + 8: return launch_batch<128, 8>(maps, bt, wv.smem, st);
+    switch (q.d * 32 + bt.p[0].G) {
+        case 64 * 32 + 1: return launch_batch<64, 1>(maps, bt, wv.smem, st);
+        case 64 * 32 + 2: return launch_batch<64, 2>(maps, bt, wv.smem, st);
+        case 64 * 32 + 4: return launch_batch<64, 4>(maps, bt, wv.smem, st);
+        case 64 * 32 + 8: return launch_batch<64, 8>(maps, bt, wv.smem, st);
+        case 64 * 32 + 16: return launch_batch<64, 16>(maps, bt, wv.smem, st);
+        case 128 * 32 + 1: return launch_batch<128, 1>(maps, bt, wv.smem, st);
+        case 128 * 32 + 2: return launch_batch<128, 2>(maps, bt, wv.smem, st);
+        case 128 * 32 + 4: return launch_batch<128, 4>(maps, bt, wv.smem, st);
+        case 128 * 32 + 8: return launch_batch<128, 8>(maps, bt, wv.smem, st);
+        case 128 * 32 + 16: return launch_batch<128, 16>(maps, bt, wv.smem, st);
         default: break;
     }
     set_error("sp_score: no tensor-core kernel for d=%d G=%d", q.d, bt.p[0].G);

@@ -80,6 +80,13 @@ SHAPES = [
     (1, 16, 2, 64, 1500, 12, "bf16"),        # three passes of 4 steps
     (2, 8, 8, 64, 700, 48, "bf16"),          # G = 1: passes of 32 and 16 steps
     (1, 8, 4, 128, 5000, 30, "bf16"),        # G = 2: passes of 16 and 14 steps
+    # query heads per KV head that are not a power of two: each step's rows padded to 4, 8 or 16
+    (2, 24, 8, 128, 2000, 8, "bf16"),        # G = 3 (padded to 4): one pass
+    (1, 40, 8, 128, 3000, 8, "bf16"),        # G = 5 (padded to 8): two passes
+    (1, 28, 4, 128, 1500, 8, "bf16"),        # G = 7 (padded to 8): two passes
+    (2, 12, 2, 64, 900, 3, "bf16"),          # G = 6 (padded to 8), d = 64
+    (1, 128, 8, 128, 1000, 2, "bf16"),       # G = 16: one pass of 2 steps
+    (1, 48, 4, 64, 700, 5, "bf16"),          # G = 12 (padded to 16): three passes
 ]
 
 
@@ -107,6 +114,22 @@ def test_long_prompts_few_layers(sp, M):
     got = run_score(sp, x)
     assert sp.sp_kernel_launches() - n0 == 2
     check_importance(got, oracle.importance(x.Q_la, x.K_prompt, x.K_la), "bf16", f"M={M}")
+
+
+@pytest.mark.parametrize("H,H_kv,passes", [(24, 8, 1), (40, 8, 2), (28, 4, 2), (128, 8, 4)])
+def test_unpadded_group_sizes_run_on_tensor_cores(sp, H, H_kv, passes):
+    """G = 3, 5, 7, 16 at d = 128 with N = 8: one preparation and one scoring
+    launch per pass of 32 / G_padded steps (the general path launches 4 kernels once)."""
+    import torch
+    wl = W.Workload("t", L=2, H=H, H_kv=H_kv, d=128, M=2000, N=8, dtype="bf16", chunk=32, pool_k=3, mode="topk",
+                    keep_rate=0.1, needle_frac=0.02, run_min=16, run_max=128)
+    x = W.make_inputs(wl, seed=H * 10 + H_kv)
+    Q, K, Kla = (to_device(getattr(x, n)) for n in ("Q_la", "K_prompt", "K_la"))
+    n0 = sp.sp_kernel_launches()
+    imp = sp.score(Q, K, Kla, check=True)
+    torch.cuda.synchronize()
+    assert sp.sp_kernel_launches() - n0 == 2 * passes
+    check_importance(imp.cpu().numpy(), oracle.importance(x.Q_la, x.K_prompt, x.K_la), "bf16", f"H={H} H_kv={H_kv}")
 
 
 def test_more_steps_than_one_pass_runs_on_tensor_cores(sp):

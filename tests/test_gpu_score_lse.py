@@ -59,6 +59,8 @@ SHAPES = [
     (2, 6, 3, 72, 513, 5, "bf16"),         # general path (d = 72)
     (2, 32, 8, 128, 2500, 16, "bf16"),     # two tensor-core passes of 8 steps
     (1, 16, 2, 64, 900, 10, "bf16"),       # passes of 4, 4 and 2 steps
+    (2, 40, 8, 128, 1200, 8, "bf16"),      # G = 5 padded to 8: two passes
+    (1, 24, 8, 64, 1000, 6, "bf16"),       # G = 3 padded to 4
     (1, 16, 2, 256, 257, 4, "f32"),
 ]
 
