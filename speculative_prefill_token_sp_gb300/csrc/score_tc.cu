@@ -513,6 +513,7 @@ __device__ __forceinline__ void merge(float& m, float& z, float m2, float z2) {
 // ---------------------------------------------------------------------------
 
 // Block s (one per slab) of one prompt's preparation.
+template <int KB, int HV>
 __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     const __nv_bfloat16* __restrict__ Q = p.Qp;
     const __nv_bfloat16* __restrict__ Kla = p.Klap;
@@ -537,55 +538,60 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
             iv[u] = *reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d + ch * 8);
         }
     }
-    // row r (query j = r / G, head g*G + r % G) against look-ahead keys k <= j - shift:
-    // eight consecutive lanes per row, one key each (keys k, k + 8, ... folded
-    // in), every dot product from independent 16-byte loads
+    // row r (query j = r / G, head g*Gr + r % G) against look-ahead keys
+    // k <= j0 + j - shift: eight consecutive lanes per row, each with an
+    // eighth of every dot product (HV = d / 64 16-byte chunks: sub, sub + 8),
+    // the keys KB at a time with all their loads in flight, the eight parts added by
+    // shuffles; every lane of the row then holds the row's statistics
     if (!p.lse_mode) {
         const int nk = p.N_total - p.la_shift;        // look-ahead keys stored per (layer, KV head)
         const int sub = lane & 7;
-        for (int r = warp * 4 + (lane >> 3); r < kRP; r += (blockDim.x / 32) * 4) {
-            float m = -INFINITY, z = 0.f;
-            if (r < p.R && r % p.G < p.Gr) {
-                const int j = r / p.G, h = g * p.Gr + r % p.G;      // step j0 + j of the call
+        for (int r0 = warp * 4; r0 < kRP; r0 += (blockDim.x / 32) * 4) {
+            const int r = r0 + (lane >> 3);
+            const bool real = r < p.R && r % p.G < p.Gr;
+            const int j = r / p.G, h = g * p.Gr + r % p.G;          // step j0 + j of the call
+            const int nkeys = real ? max(0, p.j0 + j - p.la_shift + 1) : 0;
+            int kmax = nkeys;                                         // the warp's longest key list
+#pragma unroll
+            for (int o = 8; o < 32; o <<= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+            uint4 qa[HV];
+#pragma unroll
+            for (int t = 0; t < HV; ++t) qa[t] = make_uint4(0u, 0u, 0u, 0u);
+            if (real) {
                 const uint4* q = reinterpret_cast<const uint4*>(Q + (((size_t)j * p.L + l) * p.H + h) * p.d);
-                for (int k = sub; k <= p.j0 + j - p.la_shift; k += 8) {
-                    const uint4* kk = reinterpret_cast<const uint4*>(Kla + (((size_t)l * p.H_kv + g) * nk + k) * p.d);
-                    // four 16-byte chunks of both rows in flight at a time
+#pragma unroll
+                for (int t = 0; t < HV; ++t) qa[t] = q[sub + 8 * t];
+            }
+            const uint4* kbase = reinterpret_cast<const uint4*>(Kla + ((size_t)l * p.H_kv + g) * nk * p.d);
+            float m = -INFINITY, z = 0.f;
+            for (int k0 = 0; k0 < kmax; k0 += KB) {
+                uint4 kb[KB][HV];
+#pragma unroll
+                for (int kk = 0; kk < KB; ++kk)
+#pragma unroll
+                    for (int t = 0; t < HV; ++t)
+                        kb[kk][t] = k0 + kk < nkeys
+                                        ? kbase[(size_t)(k0 + kk) * (p.d / 8) + sub + 8 * t]
+                                        : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int kk = 0; kk < KB; ++kk) {
                     float u = 0.f;
-                    for (int c0 = 0; c0 < p.d / 8; c0 += 4) {
-                        uint4 a[4], b[4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            a[c] = q[c0 + c];
-                            b[c] = kk[c0 + c];
-                        }
+                    for (int t = 0; t < HV; ++t) {
+                        const uint32_t aw[4] = {qa[t].x, qa[t].y, qa[t].z, qa[t].w};
+                        const uint32_t bw[4] = {kb[kk][t].x, kb[kk][t].y, kb[kk][t].z, kb[kk][t].w};
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            {
-                                const uint32_t aw[4] = {a[c].x, a[c].y, a[c].z, a[c].w};
-                                const uint32_t bw[4] = {b[c].x, b[c].y, b[c].z, b[c].w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 fa =
-                                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
-                                    const float2 fb =
-                                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
-                                    u = fmaf(fa.x, fb.x, u);
-                                    u = fmaf(fa.y, fb.y, u);
-                                }
-                            }
+                        for (int e = 0; e < 4; ++e) {         // a bf16 pair widens exactly by shifts
+                            u = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), u);
+                            u = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(bw[e] & 0xffff0000u), u);
                         }
                     }
-                    merge(m, z, u * p.scale_log2e, 1.f);
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+                    if (k0 + kk < nkeys) merge(m, z, u * p.scale_log2e, 1.f);
                 }
             }
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-                const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
-                merge(m, z, m2, z2);
-            }
-            if (sub == 0) la[(size_t)s * kRP + r] = make_float2(m, z);
+            if (sub == 0 && r < kRP) la[(size_t)s * kRP + r] = make_float2(m, z);
         }
     }
 #pragma unroll
@@ -623,16 +629,20 @@ __device__ __forceinline__ void tc_prep_body(const TcParams& p, int s) {
     }
 }
 
-// (four blocks per SM: a call's 256 or so slabs, or a wave's several hundred,
-// run in one or two rounds)
-__global__ void __launch_bounds__(256, 4) tc_prep_kernel(const __grid_constant__ TcParams p) {
-    tc_prep_body(p, blockIdx.x);
+// One call (HV = d / 64): two blocks per SM, up to 128 registers a thread for
+// eight keys in flight; a call's 256 or so slabs run in one round.
+template <int HV>
+__global__ void __launch_bounds__(256, 2) tc_prep_kernel(const __grid_constant__ TcParams p) {
+    tc_prep_body<8, HV>(p, blockIdx.x);
 }
 
-// All prompts of a wave: blocks b * S .. b * S + S - 1 prepare prompt b.
+// All prompts of a wave: blocks b * S .. b * S + S - 1 prepare prompt b; four
+// blocks per SM (64 registers a thread: four keys in flight at d = 64, two at
+// d = 128), so that a wave's several hundred slabs run in one or two rounds.
+template <int HV>
 __global__ void __launch_bounds__(256, 4) tc_prep_batch_kernel(const __grid_constant__ TcBatch bt) {
     const int S = bt.p[0].S;
-    tc_prep_body(bt.p[blockIdx.x / S], blockIdx.x % S);
+    tc_prep_body<4 / HV, HV>(bt.p[blockIdx.x / S], blockIdx.x % S);
 }
 
 // ---------------------------------------------------------------------------
@@ -1638,7 +1648,8 @@ static sp_status launch_prompt(const ScoreProblem& q, int b, bool first, const K
     uint8_t* w = static_cast<uint8_t*>(ws);
     bind_prompt(q, b, first, w, w, plan);
     const TcParams& p = plan.p;
-    tc_prep_kernel<<<p.S, 256, 0, st>>>(p);
+    if (p.d == 64) tc_prep_kernel<1><<<p.S, 256, 0, st>>>(p);
+    else tc_prep_kernel<2><<<p.S, 256, 0, st>>>(p);
     SP_LAUNCH_CHECK();
     switch (q.d * 32 + p.G) {
         case 64 * 32 + 1: return launch_kernel<64, 1>(maps, p, st);
@@ -1671,7 +1682,8 @@ static sp_status launch_wave(const ScoreProblem& q, Wave& wv, bool first, const 
         bt.p[i] = plan.p;
         bt.cta0[i + 1] = bt.cta0[i] + plan.p.P;
     }
-    tc_prep_batch_kernel<<<bt.nb * bt.p[0].S, 256, 0, st>>>(bt);
+    if (bt.p[0].d == 64) tc_prep_batch_kernel<1><<<bt.nb * bt.p[0].S, 256, 0, st>>>(bt);
+    else tc_prep_batch_kernel<2><<<bt.nb * bt.p[0].S, 256, 0, st>>>(bt);
     SP_LAUNCH_CHECK();
     switch (q.d * 32 + bt.p[0].G) {
         case 64 * 32 + 1: return launch_batch<64, 1>(maps, bt, wv.smem, st);
