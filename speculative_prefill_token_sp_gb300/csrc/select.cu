@@ -49,6 +49,7 @@ struct SelGeo {
     int has_boost;
     int first_n, last_n, normalize;
     double first_mult, last_mult;
+    double rcp_chunk, rcp_pool;     // RN(1/chunk), RN(1/pool_k) (IEEE division on the host)
     int64_t cu[kMaxBatch + 1];      // token offsets
     int64_t cn[kMaxBatch + 1];      // chunk offsets
     int min_tok, always_keep;       // keep rules (sp_select_rules)
@@ -61,6 +62,11 @@ __device__ __forceinline__ uint64_t order_key(double v) {
     uint64_t u = (uint64_t)__double_as_longlong(v);
     return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
+
+// Kernels launched with programmatic stream serialization may start while the
+// stream's previous kernel still runs; this waits until that kernel has
+// completed and its memory is visible (a no-op after an ordinary launch).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ int find_batch(const int64_t* cu, int B, int64_t x) {
     int lo = 0, hi = B - 1;                 // largest b with cu[b] <= x
@@ -146,6 +152,67 @@ __device__ __forceinline__ double token_score(const SelGeo& g, float v, int64_t 
     return x;
 }
 
+// RN(s / n) for a count n, with rcp = RN(1/n): q0 = RN(s * rcp) is within one
+// ulp of the quotient, the residual s - q0 * n is exact in one fma, and
+// RN(q0 + residual * rcp) is the correctly rounded quotient (Markstein's
+// theorem, as in token_score).  s is finite here and a sum of fp32 values or of
+// their means, so nothing underflows; otherwise the divide instruction.
+__device__ __forceinline__ double div_count(double s, int n, double rcp) {
+    if (!isfinite(s)) return __ddiv_rn(s, (double)n);
+    const double q0 = __dmul_rn(s, rcp);
+    const double r = __fma_rn(-q0, (double)n, s);
+    return __fma_rn(r, rcp, q0);
+}
+
+// A warp's chunk of n <= 64 plain fp32 scores: lane k holds values k and k + 32
+// (0 past n).  Their left-to-right fp64 sum is computed exactly in integers when
+// every partial sum of that chain is an fp64 number: all values finite and
+// >= 0, 2^q the smallest unit in the last place among the nonzero ones (it
+// divides every value), and the exact total below 2^(q + 53).  Every partial
+// sum is then a multiple of 2^q between 0 and the total, so each rounded
+// addition of the chain is exact and the chain's result is the exact total --
+// which integer addition gives in any order, here a warp reduction.  Otherwise
+// the chain itself runs (every lane the same, on broadcast values).  Every
+// lane returns the sum.
+__device__ __forceinline__ void decode_f32(float x, bool& ok, int& e, uint64_t& m) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t be = (u >> 23) & 255u;
+    ok = (u >> 31) == 0u && be != 255u;
+    e = be ? (int)be - 150 : -149;                         // x = m * 2^e
+    m = be ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
+}
+
+__device__ __forceinline__ double warp_chunk_sum(float x0, float x1, int n) {
+    bool ok0, ok1;
+    int e0, e1;
+    uint64_t m0, m1;
+    decode_f32(x0, ok0, e0, m0);
+    decode_f32(x1, ok1, e1, m1);
+    int qmin = min(m0 ? e0 : 1 << 20, m1 ? e1 : 1 << 20);
+    int emax = max(m0 ? e0 : -(1 << 20), m1 ? e1 : -(1 << 20));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        qmin = min(qmin, __shfl_xor_sync(0xffffffffu, qmin, o));
+        emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    }
+    bool exact = __all_sync(0xffffffffu, ok0 && ok1);
+    if (exact && emax < qmin) return 0.0;                  // every value is +0
+    exact = exact && emax - qmin <= 29;                    // every term below 2^53
+    if (exact) {
+        uint64_t S = (m0 ? m0 << (e0 - qmin) : 0ull) + (m1 ? m1 << (e1 - qmin) : 0ull);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        if ((S >> 53) == 0)
+            return __dmul_rn(__ull2double_rn(S), __longlong_as_double((long long)(qmin + 1023) << 52));
+    }
+    double s = 0.0;
+    for (int k = 0; k < n; ++k) {
+        const float v = __shfl_sync(0xffffffffu, k < 32 ? x0 : x1, k & 31);
+        s = __dadd_rn(s, (double)v);
+    }
+    return s;
+}
+
 // (1) chunk sums (left to right from 0.0) and means (one divide).
 // Sum (left to right from 0.0) and mean (one divide) of global chunk gc;
 // sixteen loads in flight ahead of the additions.
@@ -155,6 +222,7 @@ __device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __r
     const int64_t c = gc - g.cn[b];
     const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
     const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
+    const int n = (int)(hi - lo);
     NormCoef mmb = {0.0, 0.0, 0.0, 1};
     if (g.has_boost && g.normalize) mmb = mm[b];
     double s = 0.0;
@@ -168,7 +236,7 @@ __device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __r
     }
     for (; i < hi; ++i) s = __dadd_rn(s, token_score(g, imp[m0 + i], i, Mb, mmb));
     sum = s;
-    mean = __ddiv_rn(s, (double)(hi - lo));
+    mean = n == g.chunk ? div_count(s, n, g.rcp_chunk) : __ddiv_rn(s, (double)n);
 }
 
 __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const NormCoef* __restrict__ mm,
@@ -220,7 +288,63 @@ __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kern
     const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
     double s = 0.0;
     for (int64_t t = lo; t <= hi; ++t) s = __dadd_rn(s, win[threadIdx.x + r + (t - c)]);
-    pooled[gc] = __ddiv_rn(s, (double)(hi - lo + 1));
+    const int cnt = (int)(hi - lo + 1);
+    pooled[gc] = cnt == g.pool_k ? div_count(s, cnt, g.rcp_pool) : __ddiv_rn(s, (double)cnt);
+}
+
+// (1+2) for plain fp32 scores (no normalisation or boost) in chunks of up to 64
+// tokens: one warp per chunk (one coalesced load, the exact sum of
+// warp_chunk_sum), kPoolWarps chunks per block of which the first and last r =
+// (pool_k - 1) / 2 are the halo of the block's kPoolWarps - 2r pooled outputs
+// (their means are computed again by the neighbouring block, with the same
+// operations).  Pooling as in chunk_pool_kernel.  Also clears the status header.
+constexpr int kPoolWarps = 32;
+constexpr int kMaxWarpPoolHalo = 8;
+__global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const SelGeo g, const float* __restrict__ imp,
+                                                                       double* __restrict__ sums,
+                                                                       double* __restrict__ means,
+                                                                       double* __restrict__ pooled,
+                                                                       int32_t* __restrict__ hdr) {
+    __shared__ double win[kPoolWarps];
+    wait_prior_grid();
+    if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
+    const int64_t total = g.cn[g.B];
+    const int r = (g.pool_k - 1) / 2, outs = kPoolWarps - 2 * r;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t gc0 = (int64_t)blockIdx.x * outs;
+    const int64_t gc = gc0 - r + w;
+    if (gc >= 0 && gc < total) {
+        const int b = find_batch(g.cn, g.B, gc);
+        const int64_t c = gc - g.cn[b];
+        const int64_t t0 = g.cu[b], Mb = g.cu[b + 1] - t0;
+        const int64_t lo = c * g.chunk;
+        const int n = (int)min((int64_t)g.chunk, Mb - lo);
+        const float* src = imp + t0 + lo;
+        const float x0 = lane < n ? src[lane] : 0.f;
+        const float x1 = lane + 32 < n ? src[lane + 32] : 0.f;
+        const double sum = warp_chunk_sum(x0, x1, n);
+        const double mean = n == g.chunk ? div_count(sum, n, g.rcp_chunk) : __ddiv_rn(sum, (double)n);
+        if (lane == 0) {
+            win[w] = mean;
+            if (w >= r && w < r + outs) {
+                sums[gc] = sum;
+                means[gc] = mean;
+            }
+        }
+    }
+    if (g.pool_k <= 1) return;
+    __syncthreads();
+    const int t = threadIdx.x;
+    const int64_t gp = gc0 + t;
+    if (t >= outs || gp >= total) return;
+    const int b = find_batch(g.cn, g.B, gp);
+    const int64_t c = gp - g.cn[b], nc = g.cn[b + 1] - g.cn[b];
+    const int64_t lo = c - r < 0 ? 0 : c - r;
+    const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
+    double s = 0.0;
+    for (int64_t k = lo; k <= hi; ++k) s = __dadd_rn(s, win[t + r + (k - c)]);
+    const int cnt = (int)(hi - lo + 1);
+    pooled[gp] = cnt == g.pool_k ? div_count(s, cnt, g.rcp_pool) : __ddiv_rn(s, (double)cnt);
 }
 
 // (2) centred average pool over the prompt's own chunks; edges average in-range
@@ -232,7 +356,8 @@ __device__ __forceinline__ double pooled_at(const SelGeo& g, const double* __res
     const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
     double s = 0.0;
     for (int64_t t = lo; t <= hi; ++t) s = __dadd_rn(s, means[c0 + t]);
-    return __ddiv_rn(s, (double)(hi - lo + 1));
+    const int cnt = (int)(hi - lo + 1);
+    return cnt == g.pool_k ? div_count(s, cnt, g.rcp_pool) : __ddiv_rn(s, (double)cnt);
 }
 
 __global__ void pool_kernel(const SelGeo g, const double* __restrict__ means, double* __restrict__ pooled) {
@@ -387,6 +512,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
     const int nc = (int)(g.cn[b + 1] - c0);
     const int64_t Mb = g.cu[b + 1] - g.cu[b];
     const int tid = threadIdx.x;
+    wait_prior_grid();
     if (nc == 0) {
         if (tid == 0) n_kept[b] = 0;
         return;
@@ -719,6 +845,28 @@ SelLayout sel_layout(const SelectProblem& p) {
 
 size_t select_ws_bytes(const SelectProblem& p) { return sel_layout(p).total; }
 
+namespace {
+// A launch that may be scheduled while the stream's previous kernel still runs
+// (programmatic stream serialization); the kernel waits for that kernel with
+// wait_prior_grid() before it reads or writes memory.  It hides the launch and
+// the block start-up behind the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_early(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                         Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+}  // namespace
+
 sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     if (p.B > kMaxBatch) {
         set_error("sp_select: batch of %d prompts exceeds the supported %d", p.B, kMaxBatch);
@@ -734,6 +882,8 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     g.has_boost = p.has_boost ? 1 : 0;
     g.first_n = p.boost.first_n; g.last_n = p.boost.last_n; g.normalize = p.boost.normalize;
     g.first_mult = p.boost.first_mult; g.last_mult = p.boost.last_mult;
+    g.rcp_chunk = 1.0 / (double)p.chunk;
+    g.rcp_pool = 1.0 / (double)p.pool_k;
     g.min_tok = p.has_rules ? p.rules.min_tok : 0;
     g.always_keep = p.has_rules ? p.rules.always_keep : 0;
     g.max_keep = p.has_rules ? p.rules.max_keep : 0;
@@ -766,7 +916,16 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
         // small blocks: the fixed-order fp64 sums run on as many SMs as possible
         int32_t* hdr = normalize ? nullptr : static_cast<int32_t*>(ws);
         const bool pool = p.mode == SP_SELECT_TOPK && p.pool_k > 1;
-        if (pool && (p.pool_k - 1) / 2 <= kMaxPoolHalo) {
+        const int r = pool ? (p.pool_k - 1) / 2 : 0;
+        if (!p.has_boost && p.chunk <= 64 && r <= kMaxWarpPoolHalo) {
+            // plain scores in chunks of up to 64 tokens: a warp per chunk
+            SelGeo gw = g;
+            if (!pool) gw.pool_k = 1;
+            const int outs = kPoolWarps - 2 * r;
+            SP_CUDA_TRY(launch_early(chunk_pool_warp_kernel, (unsigned)((total + outs - 1) / outs), kPoolWarps * 32, 0,
+                                     st, gw, p.importance, sums, means, pooled, hdr));
+            SP_LAUNCH_CHECK();
+        } else if (pool && (p.pool_k - 1) / 2 <= kMaxPoolHalo) {
             const int threads = (kPoolBlock + (p.pool_k - 1) + 31) / 32 * 32;     // 64 + 2r means, whole warps
             chunk_pool_kernel<<<(unsigned)((total + kPoolBlock - 1) / kPoolBlock), threads, 0, st>>>(
                 g, p.importance, mm, sums, means, pooled, hdr);
@@ -789,7 +948,8 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     }
     SP_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)std::max<size_t>(dyn, 0)));
-    select_kernel<<<p.B, kSelThreads, dyn, st>>>(g, sums, means, pooled, flags, offs, p.kept_pos, p.n_kept);
+    SP_CUDA_TRY(launch_early(select_kernel, (unsigned)p.B, kSelThreads, dyn, st, g, (const double*)sums,
+                             (const double*)means, (const double*)pooled, flags, offs, p.kept_pos, p.n_kept));
     SP_LAUNCH_CHECK();
     // positions not written by the selection kernel: chunks above kInlinePosChunk
     // tokens, or top-K prompts too long for the in-register path

@@ -156,3 +156,104 @@ def test_pipeline_selection_bit_exact_on_gpu_importance(sp, name):
         # the kept count of the top-K rule: kc full chunks (no partial chunk at these sizes)
         nc = -(-wl.M // wl.chunk)
         assert n == oracle.keep_count(nc, wl.keep_rate) * wl.chunk
+
+
+# ---------------------------------------------------------------------------
+# Chunk sums, means and pooled scores themselves, bit for bit.  Plain fp32
+# chunks of up to 64 values are summed exactly in integers when every partial
+# sum of the left-to-right chain is an fp64 number, and by the chain otherwise;
+# these inputs reach both, and the edges between them.  The test reads the
+# three arrays from the selection workspace: after the 256-byte status header,
+# the per-prompt normalisation coefficients, then sums[nc], means[nc] and
+# pooled[nc], each block aligned to 256 bytes.
+# ---------------------------------------------------------------------------
+
+def _ws_arrays(ws, nc, B=1):
+    al = lambda x: (x + 255) // 256 * 256
+    off = al(256 + 32 * max(B, 1))
+    raw = ws.cpu().numpy()
+    out = []
+    for _ in range(3):
+        out.append(raw[off: off + 8 * nc].view(np.float64).copy())
+        off = al(off + 8 * nc)
+    return out                                            # sums, means, pooled
+
+
+def _edge53(M, chunk, rng):
+    """Chunks whose exact total sits just below or just above 2^53 units of the
+    smallest value's last place: one value 2^(q+23) and two or three values
+    (2^24 - 1) * 2^(q+28), the rest zero."""
+    x = np.zeros(M, dtype=np.float32)
+    for c in range(M // chunk):
+        q = int(rng.integers(-60, -30))
+        big = np.float32(np.ldexp(float((1 << 24) - 1), q + 28))
+        x[c * chunk] = np.float32(np.ldexp(1.0, q + 23))
+        nbig = 2 + (c % 2)
+        for t in range(nbig):
+            x[c * chunk + 1 + t] = big
+        rng.shuffle(x[c * chunk: (c + 1) * chunk])
+    return x
+
+
+def _chunk_inputs(kind, M, chunk, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "narrow":        # within 2^10 of each other: the exact path
+        return rng.uniform(1e-3, 1.0, M).astype(np.float32)
+    if kind == "wide":          # log-uniform over 2^-100 .. 1: mostly the chain
+        return np.exp2(rng.uniform(-100, 0, M)).astype(np.float32)
+    if kind == "subnormal":     # fp32 subnormals beside small normals, some zeros
+        x = (rng.integers(0, 1 << 23, M).astype(np.uint32)).view(np.float32).copy()
+        x[rng.random(M) < 0.3] = np.float32(2.0 ** -120)
+        x[rng.random(M) < 0.2] = 0.0
+        return x
+    if kind == "zeros":         # whole chunks of zeros and scattered zeros
+        x = rng.uniform(0.0, 1.0, M).astype(np.float32)
+        x[rng.random(M) < 0.5] = 0.0
+        x[: 3 * chunk] = 0.0
+        return x
+    if kind == "signed":        # negative values and a negative zero: the chain
+        x = rng.normal(0.0, 1.0, M).astype(np.float32)
+        x[min(5, M - 1)] = np.float32(-0.0)
+        return x
+    if kind == "edge53":
+        return _edge53(M, chunk, rng)
+    raise ValueError(kind)
+
+
+CHUNK_CASES = [
+    # (kind, M, chunk, pool_k)
+    ("narrow", 32 * 300, 32, 3),
+    ("narrow", 64 * 200 + 17, 64, 3),
+    ("narrow", 48 * 100 + 5, 48, 5),
+    ("narrow", 17 * 99, 17, 7),
+    ("narrow", 65 * 50 + 3, 65, 3),
+    ("narrow", 1000, 1, 3),
+    ("wide", 32 * 300 + 9, 32, 3),
+    ("wide", 64 * 100, 64, 1),
+    ("subnormal", 32 * 200, 32, 3),
+    ("subnormal", 64 * 100 + 33, 64, 5),
+    ("zeros", 32 * 100, 32, 3),
+    ("signed", 32 * 100 + 1, 32, 3),
+    ("signed", 64 * 60, 64, 3),
+    ("edge53", 32 * 200, 32, 3),
+    ("edge53", 64 * 100, 64, 3),
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_CASES, ids=lambda c: f"{c[0]}-M{c[1]}c{c[2]}k{c[3]}")
+def test_chunk_sums_means_pooled_bit_exact(sp, case):
+    import torch
+    kind, M, chunk, pool_k = case
+    imp = _chunk_inputs(kind, M, chunk, seed=M + chunk)
+    ws = torch.zeros(sp.sp_select_workspace_size(M, chunk), dtype=torch.uint8, device="cuda")
+    sp.select(torch.from_numpy(imp).cuda(), chunk, pool_k, "topk", 0.3, ws=ws)
+    torch.cuda.synchronize()
+    nc = (M + chunk - 1) // chunk
+    sums, means, pooled = _ws_arrays(ws, nc)
+    want_sums, _ = oracle.chunk_sums(imp, chunk)
+    want_means = oracle.chunk_means(imp, chunk)
+    assert np.array_equal(sums.view(np.uint64), want_sums.view(np.uint64)), kind
+    assert np.array_equal(means.view(np.uint64), want_means.view(np.uint64)), kind
+    if pool_k > 1:
+        want_pooled = oracle.avg_pool(want_means, pool_k)
+        assert np.array_equal(pooled.view(np.uint64), want_pooled.view(np.uint64)), kind
