@@ -68,6 +68,16 @@ __device__ __forceinline__ uint64_t order_key(double v) {
 // completed and its memory is visible (a no-op after an ordinary launch).
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Prompt offsets from the parameter block.  Reading a parameter array at a
+// runtime index is slow on the first touch (microseconds); a single prompt --
+// the common call -- reads entries 0 and 1 at fixed offsets instead.
+__device__ __forceinline__ int64_t geo_cu(const SelGeo& g, int i) {
+    return g.B == 1 ? (i == 0 ? g.cu[0] : g.cu[1]) : g.cu[i];
+}
+__device__ __forceinline__ int64_t geo_cn(const SelGeo& g, int i) {
+    return g.B == 1 ? (i == 0 ? g.cn[0] : g.cn[1]) : g.cn[i];
+}
+
 __device__ __forceinline__ int find_batch(const int64_t* cu, int B, int64_t x) {
     int lo = 0, hi = B - 1;                 // largest b with cu[b] <= x
     while (lo < hi) {
@@ -90,7 +100,7 @@ __global__ void __launch_bounds__(1024) minmax_kernel(const SelGeo g, const floa
                                                       NormCoef* __restrict__ mm, int32_t* __restrict__ hdr) {
     const int b = blockIdx.x;
     if (hdr != nullptr && b == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
+    const int64_t m0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - m0;
     float mn = INFINITY, mx = -INFINITY;
     for (int64_t i = threadIdx.x; i < Mb; i += blockDim.x) {
         float v = imp[m0 + i];
@@ -219,8 +229,8 @@ __device__ __forceinline__ double warp_chunk_sum(float x0, float x1, int n) {
 __device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __restrict__ imp,
                                                const NormCoef* __restrict__ mm, int64_t gc, double& sum, double& mean) {
     const int b = find_batch(g.cn, g.B, gc);
-    const int64_t c = gc - g.cn[b];
-    const int64_t m0 = g.cu[b], Mb = g.cu[b + 1] - m0;
+    const int64_t c = gc - geo_cn(g, b);
+    const int64_t m0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - m0;
     const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
     const int n = (int)(hi - lo);
     NormCoef mmb = {0.0, 0.0, 0.0, 1};
@@ -243,7 +253,7 @@ __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, cons
                              double* __restrict__ sums, double* __restrict__ means, int32_t* __restrict__ hdr) {
     // a fresh status for the call (the workspace header)
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t total = g.cn[g.B];
+    const int64_t total = geo_cn(g, g.B);
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
          gc += (int64_t)gridDim.x * blockDim.x)
         chunk_sum_mean(g, imp, mm, gc, sums[gc], means[gc]);
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kern
                                                                 int32_t* __restrict__ hdr) {
     __shared__ double win[kPoolBlock + 2 * kMaxPoolHalo];
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t total = g.cn[g.B];
+    const int64_t total = geo_cn(g, g.B);
     const int r = (g.pool_k - 1) / 2;
     const int64_t gc0 = (int64_t)blockIdx.x * kPoolBlock;
     for (int w = threadIdx.x; w < kPoolBlock + 2 * r; w += blockDim.x) {
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kern
     const int64_t gc = gc0 + threadIdx.x;
     if (threadIdx.x >= kPoolBlock || gc >= total) return;
     const int b = find_batch(g.cn, g.B, gc);
-    const int64_t c = gc - g.cn[b], nc = g.cn[b + 1] - g.cn[b];
+    const int64_t c = gc - geo_cn(g, b), nc = geo_cn(g, b + 1) - geo_cn(g, b);
     const int64_t lo = c - r < 0 ? 0 : c - r;
     const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
     double s = 0.0;
@@ -308,15 +318,15 @@ __global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const 
     __shared__ double win[kPoolWarps];
     wait_prior_grid();
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t total = g.cn[g.B];
+    const int64_t total = geo_cn(g, g.B);
     const int r = (g.pool_k - 1) / 2, outs = kPoolWarps - 2 * r;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t gc0 = (int64_t)blockIdx.x * outs;
     const int64_t gc = gc0 - r + w;
     if (gc >= 0 && gc < total) {
         const int b = find_batch(g.cn, g.B, gc);
-        const int64_t c = gc - g.cn[b];
-        const int64_t t0 = g.cu[b], Mb = g.cu[b + 1] - t0;
+        const int64_t c = gc - geo_cn(g, b);
+        const int64_t t0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - t0;
         const int64_t lo = c * g.chunk;
         const int n = (int)min((int64_t)g.chunk, Mb - lo);
         const float* src = imp + t0 + lo;
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const 
     const int64_t gp = gc0 + t;
     if (t >= outs || gp >= total) return;
     const int b = find_batch(g.cn, g.B, gp);
-    const int64_t c = gp - g.cn[b], nc = g.cn[b + 1] - g.cn[b];
+    const int64_t c = gp - geo_cn(g, b), nc = geo_cn(g, b + 1) - geo_cn(g, b);
     const int64_t lo = c - r < 0 ? 0 : c - r;
     const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
     double s = 0.0;
@@ -361,11 +371,11 @@ __device__ __forceinline__ double pooled_at(const SelGeo& g, const double* __res
 }
 
 __global__ void pool_kernel(const SelGeo g, const double* __restrict__ means, double* __restrict__ pooled) {
-    const int64_t total = g.cn[g.B];
+    const int64_t total = geo_cn(g, g.B);
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
          gc += (int64_t)gridDim.x * blockDim.x) {
         const int b = find_batch(g.cn, g.B, gc);
-        const int64_t c0 = g.cn[b], nc = g.cn[b + 1] - c0;
+        const int64_t c0 = geo_cn(g, b), nc = geo_cn(g, b + 1) - c0;
         pooled[gc] = pooled_at(g, means, c0, nc, gc - c0);
     }
 }
@@ -396,6 +406,31 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
     return base + x - v;
 }
 
+// The same for 32-bit values (half the shuffles).
+__device__ __forceinline__ int block_exclusive_scan32(int v, int* sh, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = lane < nw ? sh[lane] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < nw) sh[lane] = s;
+    }
+    __syncthreads();
+    const int base = w > 0 ? sh[w - 1] : 0;
+    *total = sh[nw - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
 // Top-K of a prompt with at most kSelThreads * kRegKeys chunks: the pooled keys
 // (chunk c = q * blockDim.x + tid in key[q]) stay in registers through a radix
 // select, 8 bits per pass from the most significant, counted with
@@ -405,7 +440,7 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double* __restrict__ keys_src, int64_t c0, int nc, int64_t Mb,
                                   int kc, int* __restrict__ flags, int64_t* __restrict__ offs,
                                   int32_t* __restrict__ kept_b, int64_t* __restrict__ n_kept_b, unsigned* hist,
-                                  long long* scan_sh, uint64_t* s_prefix, int* s_remaining, int* s_done) {
+                                  long long* scan_sh, int* scan32, uint64_t* s_prefix, int* s_remaining, int* s_done) {
     const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
     const int rounds = (nc + bd - 1) / bd;
     uint64_t key[kRegKeys];
@@ -416,6 +451,7 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
     }
     uint64_t prefix = 0, pmask = 0;
     int remaining = kc;
+    bool done = false;                     // every key equal to the prefix is taken
     for (int pass = 0; pass < 8; ++pass) {
         const int shift = 56 - 8 * pass;
         for (int i = tid; i < 256; i += bd) hist[i] = 0;
@@ -423,6 +459,7 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
         __syncthreads();
 #pragma unroll
         for (int q = 0; q < kRegKeys; ++q) {
+            if (q >= rounds) break;
             const int c = q * bd + tid;
             const bool take = c < nc && (key[q] & pmask) == prefix;
             const unsigned digit = take ? (unsigned)((key[q] >> shift) & 255u) : 256u;
@@ -458,10 +495,18 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
         prefix = *s_prefix;
         remaining = *s_remaining;
         pmask |= (0xFFull << shift);
-        const bool done = *s_done != 0;
+        done = *s_done != 0;
         __syncthreads();
         if (done) break;
     }
+    // Keys above the prefix are kept, and the first `remaining` equal to it in
+    // chunk order -- all of them when the last pass found exactly that many,
+    // which needs no ranking scan.  Output offsets: an exclusive scan of the
+    // kept chunk sizes (32-bit while the prompt is below 2^31 tokens).  Each
+    // warp then writes its kept chunks' positions together, one chunk at a
+    // time, lanes over the chunk's tokens.
+    const bool narrow = Mb < (int64_t)INT32_MAX;
+    const bool inline_pos = g.chunk <= kInlinePosChunk;
     long long taken_eq = 0, running = 0;
 #pragma unroll
     for (int q = 0; q < kRegKeys; ++q) {
@@ -470,20 +515,38 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
         const bool in = c < nc;
         const uint64_t k = key[q] & pmask;
         const bool gt = in && k > prefix, eq = in && k == prefix;
-        long long tot_eq;
-        const long long rank = block_exclusive_scan(eq ? 1 : 0, scan_sh, &tot_eq);
-        const bool keep = gt || (eq && taken_eq + rank < remaining);
+        bool keep = gt || eq;
+        if (!done) {
+            long long tot_eq;
+            const long long rank = block_exclusive_scan(eq ? 1 : 0, scan_sh, &tot_eq);
+            keep = gt || (eq && taken_eq + rank < remaining);
+            taken_eq += tot_eq;
+        }
         const int64_t lo = (int64_t)c * g.chunk;
         const long long sz = keep ? (long long)(min(lo + (int64_t)g.chunk, Mb) - lo) : 0;
-        long long tot_sz;
-        const long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        long long off, tot_sz;
+        if (narrow) {
+            int t32;
+            off = block_exclusive_scan32((int)sz, scan32, &t32);
+            tot_sz = t32;
+        } else {
+            off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        }
         if (in) {
             flags[c0 + c] = keep ? 1 : 0;
             offs[c0 + c] = running + off;
-            if (keep && g.chunk <= kInlinePosChunk)
-                for (long long t = 0; t < sz; ++t) kept_b[running + off + t] = (int32_t)(lo + t);
         }
-        taken_eq += tot_eq;
+        if (inline_pos) {
+            unsigned kb = __ballot_sync(0xffffffffu, keep);
+            while (kb) {
+                const int src = __ffs(kb) - 1;
+                kb &= kb - 1;
+                const long long o = __shfl_sync(0xffffffffu, running + off, src);
+                const long long l = __shfl_sync(0xffffffffu, (long long)lo, src);
+                const int n = __shfl_sync(0xffffffffu, (int)sz, src);
+                for (int t = lane; t < n; t += 32) kept_b[o + t] = (int32_t)(l + t);
+            }
+        }
         running += tot_sz;
     }
     if (tid == 0) *n_kept_b = running;
@@ -499,6 +562,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
                                                              int64_t* __restrict__ n_kept) {
     extern __shared__ __align__(16) unsigned char dsm[];
     __shared__ long long scan_sh[32];
+    __shared__ int scan32[32];
     __shared__ unsigned hist[256];
     __shared__ uint64_t s_prefix;
     __shared__ int s_remaining;
@@ -508,9 +572,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
     __shared__ double s_block[64];
 
     const int b = blockIdx.x;
-    const int64_t c0 = g.cn[b];
-    const int nc = (int)(g.cn[b + 1] - c0);
-    const int64_t Mb = g.cu[b + 1] - g.cu[b];
+    const int64_t c0 = geo_cn(g, b);
+    const int nc = (int)(geo_cn(g, b + 1) - c0);
+    const int64_t Mb = geo_cu(g, b + 1) - geo_cu(g, b);
     const int tid = threadIdx.x;
     wait_prior_grid();
     if (nc == 0) {
@@ -524,8 +588,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         int kc = (int)ceilf(prod);
         kc = kc < 1 ? 1 : (kc > nc ? nc : kc);
         if (nc <= (int)blockDim.x * kRegKeys) {
-            topk_in_registers(g, g.pool_k > 1 ? pooled : means, c0, nc, Mb, kc, flags, offs, kept_pos + g.cu[b],
-                              n_kept + b, hist, scan_sh,
+            topk_in_registers(g, g.pool_k > 1 ? pooled : means, c0, nc, Mb, kc, flags, offs, kept_pos + geo_cu(g, b),
+                              n_kept + b, hist, scan_sh, scan32,
                               &s_prefix, &s_remaining, &s_done);
             return;
         }
@@ -709,7 +773,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
         if (in) offs[c0 + c] = running + off;
         if (keep && g.chunk <= kInlinePosChunk)
-            for (long long t = 0; t < sz; ++t) kept_pos[g.cu[b] + running + off + t] = (int32_t)(lo + t);
+            for (long long t = 0; t < sz; ++t) kept_pos[geo_cu(g, b) + running + off + t] = (int32_t)(lo + t);
         running += tot_sz;
     }
     if (tid == 0) n_kept[b] = running;
@@ -718,12 +782,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
 // (4) every token of a kept chunk writes its original position.
 __global__ void compact_kernel(const SelGeo g, const int* __restrict__ flags,
                                const int64_t* __restrict__ offs, int32_t* __restrict__ kept_pos) {
-    const int64_t T = g.cu[g.B];
+    const int64_t T = geo_cu(g, g.B);
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < T;
          t += (int64_t)gridDim.x * blockDim.x) {
         const int b = find_batch(g.cu, g.B, t);
-        const int64_t m0 = g.cu[b], i = t - m0, c = i / g.chunk;
-        const int64_t gc = g.cn[b] + c;
+        const int64_t m0 = geo_cu(g, b), i = t - m0, c = i / g.chunk;
+        const int64_t gc = geo_cn(g, b) + c;
         if (flags[gc]) kept_pos[m0 + offs[gc] + (i - c * g.chunk)] = (int32_t)i;
     }
 }
@@ -744,8 +808,8 @@ __global__ void __launch_bounds__(1024) rules_kernel(const SelGeo g, const int* 
     __shared__ int n_extra;
     __shared__ int64_t total_sh;
     const int b = blockIdx.x;
-    const int64_t m0 = g.cu[b], M = g.cu[b + 1] - m0;
-    const int64_t c0 = g.cn[b], nc = g.cn[b + 1] - c0;
+    const int64_t m0 = geo_cu(g, b), M = geo_cu(g, b + 1) - m0;
+    const int64_t c0 = geo_cn(g, b), nc = geo_cn(g, b + 1) - c0;
     int32_t* kept = kept_pos + m0;
     int32_t* S = scratch + m0;                   // merged list
     const int64_t n = n_kept[b];
