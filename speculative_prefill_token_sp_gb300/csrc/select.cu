@@ -87,6 +87,38 @@ __device__ __forceinline__ int find_batch(const int64_t* cu, int B, int64_t x) {
     return lo;
 }
 
+// Offset tables of a batch for kernels that look prompts up by position: the
+// B + 1 token and chunk offsets are copied to shared memory once per block (one
+// parallel round of parameter reads; a binary search over the parameter block
+// would chain its slow reads).  A single prompt keeps the fixed-offset reads.
+// Every thread of the block calls stage_tabs before any other use.
+struct Tabs {
+    const int64_t* cu;
+    const int64_t* cn;
+};
+__device__ __forceinline__ Tabs stage_tabs(const SelGeo& g, int64_t* s_cu, int64_t* s_cn) {
+    if (g.B > 1) {
+        for (int i = threadIdx.x; i <= g.B; i += blockDim.x) {
+            s_cu[i] = g.cu[i];
+            s_cn[i] = g.cn[i];
+        }
+        __syncthreads();
+    }
+    return {s_cu, s_cn};
+}
+__device__ __forceinline__ int64_t tab_cu(const SelGeo& g, const Tabs& t, int i) {
+    return g.B == 1 ? (i == 0 ? g.cu[0] : g.cu[1]) : t.cu[i];
+}
+__device__ __forceinline__ int64_t tab_cn(const SelGeo& g, const Tabs& t, int i) {
+    return g.B == 1 ? (i == 0 ? g.cn[0] : g.cn[1]) : t.cn[i];
+}
+__device__ __forceinline__ int chunk_batch(const SelGeo& g, const Tabs& t, int64_t gc) {
+    return g.B == 1 ? 0 : find_batch(t.cn, g.B, gc);
+}
+__device__ __forceinline__ int token_batch(const SelGeo& g, const Tabs& t, int64_t i) {
+    return g.B == 1 ? 0 : find_batch(t.cu, g.B, i);
+}
+
 // Min-max normalisation of one prompt: x -> (x - mn) / (mx - mn), every score
 // 1.0 when mx == mn.  den = mx - mn (one rounding) and rcp = 1 / den (correctly
 // rounded) are computed once per prompt.
@@ -102,8 +134,9 @@ __global__ void __launch_bounds__(1024) minmax_kernel(const SelGeo g, const floa
     if (hdr != nullptr && b == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
     const int64_t m0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - m0;
     float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 8
     for (int64_t i = threadIdx.x; i < Mb; i += blockDim.x) {
-        float v = imp[m0 + i];
+        const float v = imp[m0 + i];
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
     }
@@ -226,11 +259,11 @@ __device__ __forceinline__ double warp_chunk_sum(float x0, float x1, int n) {
 // (1) chunk sums (left to right from 0.0) and means (one divide).
 // Sum (left to right from 0.0) and mean (one divide) of global chunk gc;
 // sixteen loads in flight ahead of the additions.
-__device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __restrict__ imp,
+__device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const Tabs& tb, const float* __restrict__ imp,
                                                const NormCoef* __restrict__ mm, int64_t gc, double& sum, double& mean) {
-    const int b = find_batch(g.cn, g.B, gc);
-    const int64_t c = gc - geo_cn(g, b);
-    const int64_t m0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - m0;
+    const int b = chunk_batch(g, tb, gc);
+    const int64_t c = gc - tab_cn(g, tb, b);
+    const int64_t m0 = tab_cu(g, tb, b), Mb = tab_cu(g, tb, b + 1) - m0;
     const int64_t lo = c * g.chunk, hi = min(lo + (int64_t)g.chunk, Mb);
     const int n = (int)(hi - lo);
     NormCoef mmb = {0.0, 0.0, 0.0, 1};
@@ -252,11 +285,13 @@ __device__ __forceinline__ void chunk_sum_mean(const SelGeo& g, const float* __r
 __global__ void chunk_kernel(const SelGeo g, const float* __restrict__ imp, const NormCoef* __restrict__ mm,
                              double* __restrict__ sums, double* __restrict__ means, int32_t* __restrict__ hdr) {
     // a fresh status for the call (the workspace header)
+    __shared__ int64_t s_cu[kMaxBatch + 1], s_cn[kMaxBatch + 1];
+    const Tabs tb = stage_tabs(g, s_cu, s_cn);
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t total = geo_cn(g, g.B);
+    const int64_t total = tab_cn(g, tb, g.B);
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
          gc += (int64_t)gridDim.x * blockDim.x)
-        chunk_sum_mean(g, imp, mm, gc, sums[gc], means[gc]);
+        chunk_sum_mean(g, tb, imp, mm, gc, sums[gc], means[gc]);
 }
 
 // (1+2) chunk sums and means, and the centred pool, for the block's 64 chunks:
@@ -274,15 +309,17 @@ __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kern
                                                                 double* __restrict__ pooled,
                                                                 int32_t* __restrict__ hdr) {
     __shared__ double win[kPoolBlock + 2 * kMaxPoolHalo];
+    __shared__ int64_t s_cu[kMaxBatch + 1], s_cn[kMaxBatch + 1];
+    const Tabs tb = stage_tabs(g, s_cu, s_cn);
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t total = geo_cn(g, g.B);
+    const int64_t total = tab_cn(g, tb, g.B);
     const int r = (g.pool_k - 1) / 2;
     const int64_t gc0 = (int64_t)blockIdx.x * kPoolBlock;
     for (int w = threadIdx.x; w < kPoolBlock + 2 * r; w += blockDim.x) {
         const int64_t gc = gc0 - r + w;
         if (gc < 0 || gc >= total) continue;
         double sm, mn;
-        chunk_sum_mean(g, imp, mm, gc, sm, mn);
+        chunk_sum_mean(g, tb, imp, mm, gc, sm, mn);
         win[w] = mn;
         if (w >= r && w < r + kPoolBlock) {
             sums[gc] = sm;
@@ -292,8 +329,8 @@ __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kern
     __syncthreads();
     const int64_t gc = gc0 + threadIdx.x;
     if (threadIdx.x >= kPoolBlock || gc >= total) return;
-    const int b = find_batch(g.cn, g.B, gc);
-    const int64_t c = gc - geo_cn(g, b), nc = geo_cn(g, b + 1) - geo_cn(g, b);
+    const int b = chunk_batch(g, tb, gc);
+    const int64_t c = gc - tab_cn(g, tb, b), nc = tab_cn(g, tb, b + 1) - tab_cn(g, tb, b);
     const int64_t lo = c - r < 0 ? 0 : c - r;
     const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
     double s = 0.0;
@@ -316,17 +353,19 @@ __global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const 
                                                                        double* __restrict__ pooled,
                                                                        int32_t* __restrict__ hdr) {
     __shared__ double win[kPoolWarps];
+    __shared__ int64_t s_cu[kMaxBatch + 1], s_cn[kMaxBatch + 1];
+    const Tabs tb = stage_tabs(g, s_cu, s_cn);
     wait_prior_grid();
     if (hdr != nullptr && blockIdx.x == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
-    const int64_t total = geo_cn(g, g.B);
+    const int64_t total = tab_cn(g, tb, g.B);
     const int r = (g.pool_k - 1) / 2, outs = kPoolWarps - 2 * r;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t gc0 = (int64_t)blockIdx.x * outs;
     const int64_t gc = gc0 - r + w;
     if (gc >= 0 && gc < total) {
-        const int b = find_batch(g.cn, g.B, gc);
-        const int64_t c = gc - geo_cn(g, b);
-        const int64_t t0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - t0;
+        const int b = chunk_batch(g, tb, gc);
+        const int64_t c = gc - tab_cn(g, tb, b);
+        const int64_t t0 = tab_cu(g, tb, b), Mb = tab_cu(g, tb, b + 1) - t0;
         const int64_t lo = c * g.chunk;
         const int n = (int)min((int64_t)g.chunk, Mb - lo);
         const float* src = imp + t0 + lo;
@@ -347,8 +386,8 @@ __global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const 
     const int t = threadIdx.x;
     const int64_t gp = gc0 + t;
     if (t >= outs || gp >= total) return;
-    const int b = find_batch(g.cn, g.B, gp);
-    const int64_t c = gp - geo_cn(g, b), nc = geo_cn(g, b + 1) - geo_cn(g, b);
+    const int b = chunk_batch(g, tb, gp);
+    const int64_t c = gp - tab_cn(g, tb, b), nc = tab_cn(g, tb, b + 1) - tab_cn(g, tb, b);
     const int64_t lo = c - r < 0 ? 0 : c - r;
     const int64_t hi = c + r > nc - 1 ? nc - 1 : c + r;
     double s = 0.0;
@@ -371,11 +410,13 @@ __device__ __forceinline__ double pooled_at(const SelGeo& g, const double* __res
 }
 
 __global__ void pool_kernel(const SelGeo g, const double* __restrict__ means, double* __restrict__ pooled) {
-    const int64_t total = geo_cn(g, g.B);
+    __shared__ int64_t s_cu[kMaxBatch + 1], s_cn[kMaxBatch + 1];
+    const Tabs tb = stage_tabs(g, s_cu, s_cn);
+    const int64_t total = tab_cn(g, tb, g.B);
     for (int64_t gc = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gc < total;
          gc += (int64_t)gridDim.x * blockDim.x) {
-        const int b = find_batch(g.cn, g.B, gc);
-        const int64_t c0 = geo_cn(g, b), nc = geo_cn(g, b + 1) - c0;
+        const int b = chunk_batch(g, tb, gc);
+        const int64_t c0 = tab_cn(g, tb, b), nc = tab_cn(g, tb, b + 1) - c0;
         pooled[gc] = pooled_at(g, means, c0, nc, gc - c0);
     }
 }
@@ -568,7 +609,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
     __shared__ int s_remaining;
     __shared__ int s_kstar;
     __shared__ int s_done;
-    __shared__ double s_total;
+    __shared__ int s_flag[32];
+    __shared__ double s_rhs[2];
     __shared__ double s_block[64];
 
     const int b = blockIdx.x;
@@ -661,55 +703,77 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         return;
     }
 
-    // Cumulative-mass mode.  Warp 0 adds the total mass in chunk order while
-    // the other warps sort (key = descending mean, index) bitonically, gather
-    // the chunk sums in ranked order into the sort's key array and add the
-    // running mass in ranked order, keeping every prefix in place; the cut is
-    // then found in parallel.  Both running sums stay serial (their order is
-    // part of the definition); the total's operands are loaded by the lanes
-    // 32 at a time, one block ahead of the additions.
+    // Cumulative-mass mode: rank the chunks (descending mean, then index) and
+    // keep the shortest ranked prefix whose running mass R_k, added in ranked
+    // order, reaches target = RN(tau * total), the total added in chunk order
+    // (both chains in fp64, left to right).  The two chains are not run.
+    // With every chunk sum finite and >= 0, each chain's result is within
+    // gamma_n = n u / (1 - n u) (u = 2^-53) relative of its exact sum (the
+    // error bound of recursive summation), and a tree sum or a parallel
+    // prefix sum is within gamma_L of it for its depth L <= 64.  So with
+    // E = (nc + 80) 2^-52, which covers both and the roundings of the test
+    // itself, the prefix sum P_k and total P_n from the parallel sums decide
+    //   R_k >= target  when P_k (1 - E) > tau P_n (1 + E),
+    //   R_k <  target  when P_k (1 + E) < tau P_n (1 - E).
+    // The cut is the first k not decided "below"; if that one is not decided
+    // "reached", or a sum is negative or not finite, the two chains run
+    // serially, exactly as defined.
     int P = 1;
     while (P < nc) P <<= 1;
     uint64_t* keys = reinterpret_cast<uint64_t*>(dsm);
     int* idx = reinterpret_cast<int*>(dsm + sizeof(uint64_t) * P);
     double* ranked = reinterpret_cast<double*>(keys);
-    if (tid < 32) {
-        // blocks of 32 operands pass through a shared double buffer; every lane
-        // runs the same chain on broadcast reads
-        double total = 0.0;
-        double nxt = tid < nc ? sums[c0 + tid] : 0.0;
-        for (int base = 0, half = 0; base < nc; base += 32, half ^= 1) {
-            double* buf = s_block + 32 * half;
-            buf[tid] = nxt;
-            nxt = base + 32 + tid < nc ? sums[c0 + base + 32 + tid] : 0.0;
-            __syncwarp();
-            if (base + 32 <= nc) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    double v[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = buf[16 * h + k];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) total = __dadd_rn(total, v[k]);
-                }
-            } else {
-                for (int k = 0; k < nc - base; ++k) total = __dadd_rn(total, buf[k]);
-            }
+    const int nt = (int)blockDim.x, lane = tid & 31, wid = tid >> 5;
+    // sort keys, and the check that every chunk sum is finite and >= 0 (its
+    // bits below those of +inf); fp64 work is kept to the threads that need it,
+    // fp64 throughput being low on this GPU
+    bool fine = true;
+    for (int i = tid; i < P; i += nt) {
+        if (i < nc) {
+            keys[i] = ~order_key(means[c0 + i]);
+            idx[i] = i;
+            fine = fine && (uint64_t)__double_as_longlong(sums[c0 + i]) < 0x7ff0000000000000ull;
+        } else {
+            keys[i] = ~0ull;
+            idx[i] = 0x7fffffff;
         }
-        if (tid == 0) {
-            s_total = total;
-            s_kstar = nc;                          // every chunk, if the target is never reached
-        }
-    } else {
-        const int t = tid - 32, nt = (int)blockDim.x - 32;   // the sorting threads (named barrier 1)
-        for (int i = t; i < P; i += nt) {
-            if (i < nc) { keys[i] = ~order_key(means[c0 + i]); idx[i] = i; }
-            else        { keys[i] = ~0ull; idx[i] = 0x7fffffff; }
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
+    }
+    fine = __all_sync(0xffffffffu, fine);
+    if (lane == 0) s_flag[wid] = fine ? 1 : 0;
+    if (tid == 0) { s_kstar = nc; s_done = 0; }
+    __syncthreads();
+    if (P <= nt) {
+        // one (key, index) per thread: bitonic stages with partners inside the
+        // warp by shuffles, the others through shared memory
+        uint64_t k = tid < P ? keys[tid] : ~0ull;
+        int x = tid < P ? idx[tid] : 0x7fffffff;
         for (int size = 2; size <= P; size <<= 1) {
             for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = t; i < P / 2; i += nt) {
+                uint64_t kp;
+                int xp;
+                if (stride >= 32) {
+                    __syncthreads();
+                    if (tid < P) { keys[tid] = k; idx[tid] = x; }
+                    __syncthreads();
+                    kp = tid < P ? keys[tid ^ stride] : ~0ull;
+                    xp = tid < P ? idx[tid ^ stride] : 0x7fffffff;
+                } else {
+                    kp = __shfl_xor_sync(0xffffffffu, k, stride);
+                    xp = __shfl_xor_sync(0xffffffffu, x, stride);
+                }
+                // ascending within blocks of `size` whose bit `size` is 0, descending in the others;
+                // the lower thread of a pair keeps the smaller in an ascending block
+                const bool up = (tid & size) == 0, lower = (tid & stride) == 0;
+                const bool mine_gt = k > kp || (k == kp && x > xp);
+                if (mine_gt == (up == lower)) { k = kp; x = xp; }
+            }
+        }
+        __syncthreads();
+        if (tid < P) { keys[tid] = k; idx[tid] = x; }
+    } else {
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < P / 2; i += nt) {
                     const int lo = 2 * i - (i & (stride - 1));
                     const int hi = lo + stride;
                     const bool up = (lo & size) == 0;
@@ -721,59 +785,120 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
                         idx[lo] = ib; idx[hi] = ia;
                     }
                 }
-                asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
-            }
-        }
-        for (int k = t; k < nc; k += nt) ranked[k] = sums[c0 + idx[k]];
-        asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
-        if (t == 0) {
-            double cum = 0.0;
-            int k0 = 0;
-            for (; k0 + 16 <= nc; k0 += 16) {
-                double v[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = ranked[k0 + k];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    cum = __dadd_rn(cum, v[k]);
-                    v[k] = cum;
-                }
-#pragma unroll
-                for (int k = 0; k < 16; ++k) ranked[k0 + k] = v[k];
-            }
-            for (; k0 < nc; ++k0) {
-                cum = __dadd_rn(cum, ranked[k0]);
-                ranked[k0] = cum;
+                __syncthreads();
             }
         }
     }
     __syncthreads();
-    {
-        // kstar = 1 + the first ranked position whose running mass reaches tau * total
-        const double target = __dmul_rn(g.rate, s_total);
-        for (int k = tid; k < nc; k += blockDim.x) {
-            if (ranked[k] >= target) {
-                atomicMin(&s_kstar, k + 1);
+    bool all_fine = true;
+    for (int w = 0; w < nt / 32; ++w) all_fine = all_fine && s_flag[w] != 0;
+    // prefix sums in ranked order: a contiguous segment per thread, a scan of
+    // the segment totals inside each warp that holds chunks, then across those
+    // warps; the last prefix is the total
+    const int seg = (nc + nt - 1) / nt, k0 = tid * seg, k1 = min(k0 + seg, nc);
+    const int wact = (nc + 32 * seg - 1) / (32 * seg);   // warps that hold chunks
+    double loc = 0.0, incl = 0.0;
+    if (wid < wact) {
+        for (int k = k0; k < k1; ++k) {
+            const double v = sums[c0 + idx[k]];
+            loc = k == k0 ? v : __dadd_rn(loc, v);
+        }
+        incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl = __dadd_rn(incl, y);
+        }
+        if (lane == 31) s_block[wid] = incl;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        double w_in = lane < wact ? s_block[lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, w_in, o);
+            if (lane >= o) w_in = __dadd_rn(w_in, y);
+        }
+        s_block[32 + lane] = w_in;                     // inclusive over warps
+    }
+    __syncthreads();
+    const double E = (double)(nc + 80) * 0x1p-52;
+    if (tid == 0) {
+        const double total_c = s_block[32 + wact - 1];
+        s_rhs[0] = __dmul_rn(__dmul_rn(g.rate, total_c), 1.0 + E);
+        s_rhs[1] = __dmul_rn(__dmul_rn(g.rate, total_c), 1.0 - E);
+    }
+    __syncthreads();
+    const double rhs_hi = s_rhs[0], rhs_lo = s_rhs[1];
+    if (wid < wact) {
+        // the exclusive prefix of this thread's segment: the warps before, then the lanes before
+        const double lanes_before = __shfl_up_sync(0xffffffffu, incl, 1);
+        double run = wid > 0 ? s_block[32 + wid - 1] : 0.0;
+        if (lane > 0) run = wid > 0 ? __dadd_rn(run, lanes_before) : lanes_before;
+        for (int k = k0; k < k1; ++k) {
+            const double v = sums[c0 + idx[k]];
+            run = (k == 0) ? v : __dadd_rn(run, v);
+            ranked[k] = run;                           // P_k, the prefix through position k
+            const bool below = __dmul_rn(run, 1.0 + E) < rhs_lo;
+            if (!below) {
+                atomicMin(&s_kstar, k);
                 break;
             }
         }
     }
     __syncthreads();
+    if (tid == 0) {
+        const int ka = s_kstar;                        // first position not decided "below"
+        bool decided = all_fine;
+        if (decided && ka < nc) decided = __dmul_rn(ranked[ka], 1.0 - E) > rhs_hi;
+        s_kstar = ka < nc ? ka + 1 : nc;
+        s_done = decided ? 0 : 1;                      // 1: run the chains
+    }
+    __syncthreads();
+    if (s_done) {
+        // the definition itself: the total in chunk order, then the running
+        // mass in ranked order, one thread
+        if (tid == 0) {
+            double total = 0.0;
+            for (int c = 0; c < nc; ++c) total = __dadd_rn(total, sums[c0 + c]);
+            const double target = __dmul_rn(g.rate, total);
+            double cum = 0.0;
+            int kstar = nc;
+            for (int k = 0; k < nc; ++k) {
+                cum = __dadd_rn(cum, sums[c0 + idx[k]]);
+                if (cum >= target) {
+                    kstar = k + 1;
+                    break;
+                }
+            }
+            s_kstar = kstar;
+        }
+        __syncthreads();
+    }
     const int kstar = s_kstar;
-    for (int k = tid; k < nc; k += blockDim.x) flags[c0 + idx[k]] = k < kstar ? 1 : 0;
+    for (int k = tid; k < nc; k += nt) flags[c0 + idx[k]] = k < kstar ? 1 : 0;
     __syncthreads();
     long long running = 0;
-    for (int base = 0; base < nc; base += blockDim.x) {
+    for (int base = 0; base < nc; base += nt) {
         const int c = base + tid;
         const bool in = c < nc;
         const bool keep = in && flags[c0 + c] != 0;
         const int64_t lo = (int64_t)c * g.chunk;
         const long long sz = keep ? (long long)(min(lo + (int64_t)g.chunk, Mb) - lo) : 0;
         long long tot_sz;
-        long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        const long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
         if (in) offs[c0 + c] = running + off;
-        if (keep && g.chunk <= kInlinePosChunk)
-            for (long long t = 0; t < sz; ++t) kept_pos[geo_cu(g, b) + running + off + t] = (int32_t)(lo + t);
+        if (g.chunk <= kInlinePosChunk) {
+            unsigned kb = __ballot_sync(0xffffffffu, keep);
+            while (kb) {
+                const int src = __ffs(kb) - 1;
+                kb &= kb - 1;
+                const long long o = __shfl_sync(0xffffffffu, running + off, src);
+                const long long l = __shfl_sync(0xffffffffu, (long long)lo, src);
+                const int n = __shfl_sync(0xffffffffu, (int)sz, src);
+                for (int t = lane; t < n; t += 32) kept_pos[geo_cu(g, b) + o + t] = (int32_t)(l + t);
+            }
+        }
         running += tot_sz;
     }
     if (tid == 0) n_kept[b] = running;
@@ -782,12 +907,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
 // (4) every token of a kept chunk writes its original position.
 __global__ void compact_kernel(const SelGeo g, const int* __restrict__ flags,
                                const int64_t* __restrict__ offs, int32_t* __restrict__ kept_pos) {
-    const int64_t T = geo_cu(g, g.B);
+    __shared__ int64_t s_cu[kMaxBatch + 1], s_cn[kMaxBatch + 1];
+    const Tabs tb = stage_tabs(g, s_cu, s_cn);
+    const int64_t T = tab_cu(g, tb, g.B);
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < T;
          t += (int64_t)gridDim.x * blockDim.x) {
-        const int b = find_batch(g.cu, g.B, t);
-        const int64_t m0 = geo_cu(g, b), i = t - m0, c = i / g.chunk;
-        const int64_t gc = geo_cn(g, b) + c;
+        const int b = token_batch(g, tb, t);
+        const int64_t m0 = tab_cu(g, tb, b), i = t - m0, c = i / g.chunk;
+        const int64_t gc = tab_cn(g, tb, b) + c;
         if (flags[gc]) kept_pos[m0 + offs[gc] + (i - c * g.chunk)] = (int32_t)i;
     }
 }

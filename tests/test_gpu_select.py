@@ -257,3 +257,45 @@ def test_chunk_sums_means_pooled_bit_exact(sp, case):
     if pool_k > 1:
         want_pooled = oracle.avg_pool(want_means, pool_k)
         assert np.array_equal(pooled.view(np.uint64), want_pooled.view(np.uint64)), kind
+
+
+# ---------------------------------------------------------------------------
+# Cumulative-mass cut.  The kernel decides R_k >= target from parallel sums
+# with an error margin and runs the two serial fp64 chains of the definition
+# only when the margin does not decide; these inputs reach both: exact ties
+# between the running mass and the target, a target reached only at the last
+# chunk (tau = 1), all-zero and negative chunk sums, and ordinary prompts.
+# ---------------------------------------------------------------------------
+
+MASS_CASES = [
+    # (kind, M, chunk, tau, boost)
+    ("zeros", 3000, 32, 0.85, None),
+    ("constant", 3200, 32, 0.5, None),
+    ("constant", 3200, 32, 0.85, None),
+    ("constant", 640, 32, 1.0, None),
+    ("dyadic", 8000, 16, 0.75, None),
+    ("negative", 5000, 32, 0.85, (0, 1.0, 0, 1.0, 0)),
+    ("random", 20000, 32, 1.0, W.V3_BOOST),
+    ("random", 200000, 16, 0.85, W.V3_BOOST),
+    ("random", 30000, 32, 0.3, (64, 1.5, 128, 1.3, 0)),
+]
+
+
+def _mass_inputs(kind, M, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "zeros":
+        return np.zeros(M, dtype=np.float32)
+    if kind == "constant":
+        return np.full(M, 0.125, dtype=np.float32)
+    if kind == "dyadic":
+        return (rng.integers(0, 4, M) * 0.25).astype(np.float32)
+    if kind == "negative":
+        return rng.normal(0.0, 1.0, M).astype(np.float32)
+    return (rng.random(M) * 1e-3).astype(np.float32)
+
+
+@pytest.mark.parametrize("case", MASS_CASES, ids=lambda c: f"{c[0]}-M{c[1]}c{c[2]}t{c[3]}")
+def test_mass_cut_bit_exact(sp, case):
+    kind, M, chunk, tau, boost = case
+    imp = _mass_inputs(kind, M, seed=M + chunk)
+    assert_same(sp, imp, chunk, 1, "mass", tau, boost)
