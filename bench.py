@@ -48,7 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="llama8b-bf16-32k",
-                    help="single-prompt workload (default: the 8B shape at M = 32K)")
+                    help="workload (default: the 8B shape at M = 32K); a batch workload (the v3 batch) "
+                         "runs with --bare only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the other workloads' timings (8K, 128K, the v3 batch, tiny)")
@@ -309,17 +310,12 @@ def upload(a, dev):
 PER_WORKLOAD = ("tiny-f32-512", "llama8b-bf16-8k", "llama8b-bf16-128k", "v3-batch16-0.8b-bf16")
 
 
-def time_workload(sp, name: str, dev, flush, stream, reps: int, peak: float) -> dict:
-    """One step of the named workload (sp_score + sp_select, or the varlen pair
-    for a batch) and its scoring call alone, each `reps` times with L2 flushed
-    before every call; median milliseconds per step and per scoring call."""
-    import numpy as np
+def workload_calls(sp, wl, x, dev, stream):
+    """The scoring and selection calls of one step of a workload (sp_score +
+    sp_select, or the varlen pair for a batch) on device-resident inputs:
+    (score_call, select_call, tokens, scoring workspace, buffers to free)."""
     import torch
 
-    import workloads as W
-
-    wl = W.BY_NAME[name]
-    x = W.make_workload_inputs(name)
     dt = sp.SP_BF16 if wl.dtype == "bf16" else sp.SP_F32
     rate = wl.keep_rate if wl.mode == "topk" else wl.mass
     mode = sp.SP_SELECT_TOPK if wl.mode == "topk" else sp.SP_SELECT_MASS
@@ -369,6 +365,20 @@ def time_workload(sp, name: str, dev, flush, stream, reps: int, peak: float) -> 
                              stream)
             if s != sp.SP_OK:
                 raise sp.SpError(s, sp.sp_last_error())
+    return score_call, select_call, T, ws_s, [Q, K, Kla, imp, kept, n_kept, ws_s, ws_k]
+
+
+def time_workload(sp, name: str, dev, flush, stream, reps: int, peak: float) -> dict:
+    """One step of the named workload (sp_score + sp_select, or the varlen pair
+    for a batch) and its scoring call alone, each `reps` times with L2 flushed
+    before every call; median milliseconds per step and per scoring call."""
+    import torch
+
+    import workloads as W
+
+    wl = W.BY_NAME[name]
+    x = W.make_workload_inputs(name)
+    score_call, select_call, T, ws_s, bufs = workload_calls(sp, wl, x, dev, stream)
     del x
 
     def timed(fn):
@@ -404,7 +414,7 @@ def time_workload(sp, name: str, dev, flush, stream, reps: int, peak: float) -> 
            "launch_ms": score_ms, "launches_per_call": score_launches, "algorithmic_bytes": k_bytes,
            "achieved_gbs": achieved, "frac": achieved / peak, "traffic": recorded_traffic(name),
            "timing": f"median of {reps} steps and of {reps} scoring calls, L2 flushed before each"}
-    del Q, K, Kla, imp, kept, n_kept, ws_s, ws_k
+    del bufs, ws_s
     torch.cuda.empty_cache()
     return out
 
@@ -432,7 +442,30 @@ def run_gpu(args) -> None:
     B.build()
     dev = torch.device("cuda", local)
     wl = W.BY_NAME[args.workload]
-    assert wl.batch == 1, "bench runs a single-prompt workload"
+    stream = torch.cuda.current_stream(dev)
+    if wl.batch > 1:
+        # a batch (sp_score_varlen + sp_select_varlen) only as a bare timing loop;
+        # the contract line above measures a single-prompt workload
+        assert args.bare and not args.layers, "a batch workload runs with --bare only"
+        score_call, select_call, _, ws_s, _bufs = workload_calls(sp, wl, W.make_workload_inputs(wl.name), dev, stream)
+        for _ in range(max(args.warmup, 3)):
+            score_call()
+            select_call()
+        torch.cuda.synchronize()
+        st = sp.sp_workspace_status(ws_s, stream)
+        if st != sp.SP_OK:
+            raise sp.SpError(st, sp.sp_last_error())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            score_call()
+            select_call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"bare": True, "workload": wl.name, "prompts": wl.batch, "steps": args.steps,
+                              "ms_per_step": e0.elapsed_time(e1) / args.steps}), flush=True)
+        return
     x = W.make_inputs(wl, wl.seed)
     if args.layers:
         assert args.bare and 0 < args.layers <= wl.L, "--layers takes --bare and at most the workload's layers"
@@ -451,7 +484,6 @@ def run_gpu(args) -> None:
     ws_s = torch.empty(ws_s_bytes, dtype=torch.uint8, device=dev)
     ws_k = torch.empty(ws_k_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
     rate = wl.keep_rate if wl.mode == "topk" else wl.mass
     mode = sp.SP_SELECT_TOPK if wl.mode == "topk" else sp.SP_SELECT_MASS
 
