@@ -8,24 +8,28 @@
 // float product, ascending output), "v3 Improvements" (structural boost,
 // cumulative attention mass) and "v3.1: Score Normalization".
 //
-// Every fp64 step uses explicitly rounded intrinsics (__dadd_rn, __dmul_rn,
-// __ddiv_rn) in a fixed order -- token scores left to right inside a chunk,
-// pooled windows left to right, the total mass in chunk order and the running
-// mass in ranked order -- so the result equals any IEEE-754 evaluation of the
-// same steps bit for bit.
+// Every result equals the fixed-order fp64 evaluation of the definition --
+// token scores left to right inside a chunk, pooled windows left to right, the
+// total mass in chunk order and the running mass in ranked order, each step
+// rounded to nearest -- bit for bit.  Where a shortcut is taken it is one that
+// provably gives that same result: an integer sum where every partial sum of
+// the chain is exact, a correctly rounded division by a reciprocal and one
+// correction, and a cumulative-mass cut decided from parallel sums only when
+// the summation error bound decides it (the chains run otherwise).
 //
 // Kernels: (0) per-prompt min/max (normalisation only); (1+2) chunk sums and
-// means with the pooled scores in one multi-block pass (chunk_pool_kernel:
-// each block pools its chunks from a shared-memory window with a halo), or
-// chunk sums (1) and a separate pool pass (2) for windows wider than the halo;
-// (3) one CTA per prompt: radix select of exactly kc chunks on (score desc,
-// index asc) with the keys in registers (prompts of up to 4096 chunks; longer
-// ones read them from memory each pass), or a bitonic sort of (mean desc,
-// index asc) and the running-mass cut (the total and the ranked running sums
-// in two warps side by side); then the exclusive scan of kept chunk
-// sizes and, for chunks of up to 256 tokens, the kept positions themselves;
-// (4) compaction of the kept positions for larger chunks or longer prompts;
-// (5) the guide's v2 keep rules (sp_select_rules).
+// means with the pooled scores in one multi-block pass: a warp per chunk for
+// plain scores in chunks of up to 64 tokens (chunk_pool_warp_kernel), a thread
+// per chunk otherwise (chunk_pool_kernel; each block pools its chunks from a
+// shared-memory window with a halo), or chunk sums (1) and a separate pool
+// pass (2) for windows wider than the halo; (3) one CTA per prompt: radix
+// select of exactly kc chunks on (score desc, index asc) with the keys in
+// registers (prompts of up to 4096 chunks; longer ones read them from memory
+// each pass), or a bitonic sort of (mean desc, index asc) and the
+// running-mass cut; then the exclusive scan of kept chunk sizes and, for
+// chunks of up to 256 tokens, the kept positions themselves; (4) compaction of
+// the kept positions for larger chunks or longer prompts; (5) the guide's v2
+// keep rules (sp_select_rules).
 #include "sp_common.cuh"
 
 #include <math.h>
