@@ -598,6 +598,8 @@ __device__ __forceinline__ void topk_in_registers(const SelGeo& g, const double*
 }
 
 // (3) per-prompt selection.  Writes keep flags, kept-size offsets and n_kept.
+// (one instantiation per mode: each launch carries only its mode's code)
+template <int kMode>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, const double* __restrict__ sums,
                                                              const double* __restrict__ means,
                                                              const double* __restrict__ pooled,
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         return;
     }
 
-    if (g.mode == SP_SELECT_TOPK) {
+    if constexpr (kMode == SP_SELECT_TOPK) {
         // kc = max(1, ceil(f32(nc) * f32(keep_rate))), at most nc.
         const float prod = (float)nc * (float)g.rate;
         int kc = (int)ceilf(prod);
@@ -1141,9 +1143,10 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
         while (P < p.max_nc) P <<= 1;
         dyn = (sizeof(uint64_t) + sizeof(int)) * (size_t)P;
     }
-    SP_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto* sel_kern = p.mode == SP_SELECT_MASS ? select_kernel<SP_SELECT_MASS> : select_kernel<SP_SELECT_TOPK>;
+    SP_CUDA_TRY(cudaFuncSetAttribute(sel_kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)std::max<size_t>(dyn, 0)));
-    SP_CUDA_TRY(launch_early(select_kernel, (unsigned)p.B, kSelThreads, dyn, st, g, (const double*)sums,
+    SP_CUDA_TRY(launch_early(sel_kern, (unsigned)p.B, kSelThreads, dyn, st, g, (const double*)sums,
                              (const double*)means, (const double*)pooled, flags, offs, p.kept_pos, p.n_kept));
     SP_LAUNCH_CHECK();
     // positions not written by the selection kernel: chunks above kInlinePosChunk
