@@ -351,7 +351,14 @@ __global__ void __launch_bounds__(kPoolBlock + 2 * kMaxPoolHalo) chunk_pool_kern
 // operations).  Pooling as in chunk_pool_kernel.  Also clears the status header.
 constexpr int kPoolWarps = 32;
 constexpr int kMaxWarpPoolHalo = 8;
+// kBoost: boosted (and normalised) token scores, which are fp64 and get no
+// integer sum.  Their fp64 work is spread so that every warp instruction
+// carries 32 lanes: each warp computes its chunk's token scores one token per
+// lane into shared memory, then warp 0 runs the 32 chunks' chains, one chunk
+// per lane (a warp-wide fp64 instruction costs the same with 1 or 32 lanes).
+template <bool kBoost>
 __global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const SelGeo g, const float* __restrict__ imp,
+                                                                       const NormCoef* __restrict__ mm,
                                                                        double* __restrict__ sums,
                                                                        double* __restrict__ means,
                                                                        double* __restrict__ pooled,
@@ -366,22 +373,55 @@ __global__ void __launch_bounds__(kPoolWarps * 32) chunk_pool_warp_kernel(const 
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t gc0 = (int64_t)blockIdx.x * outs;
     const int64_t gc = gc0 - r + w;
-    if (gc >= 0 && gc < total) {
-        const int b = chunk_batch(g, tb, gc);
-        const int64_t c = gc - tab_cn(g, tb, b);
-        const int64_t t0 = tab_cu(g, tb, b), Mb = tab_cu(g, tb, b + 1) - t0;
-        const int64_t lo = c * g.chunk;
-        const int n = (int)min((int64_t)g.chunk, Mb - lo);
-        const float* src = imp + t0 + lo;
-        const float x0 = lane < n ? src[lane] : 0.f;
-        const float x1 = lane + 32 < n ? src[lane + 32] : 0.f;
-        const double sum = warp_chunk_sum(x0, x1, n);
-        const double mean = n == g.chunk ? div_count(sum, n, g.rcp_chunk) : __ddiv_rn(sum, (double)n);
-        if (lane == 0) {
-            win[w] = mean;
-            if (w >= r && w < r + outs) {
-                sums[gc] = sum;
-                means[gc] = mean;
+    if constexpr (!kBoost) {
+        if (gc >= 0 && gc < total) {
+            const int b = chunk_batch(g, tb, gc);
+            const int64_t c = gc - tab_cn(g, tb, b);
+            const int64_t t0 = tab_cu(g, tb, b), Mb = tab_cu(g, tb, b + 1) - t0;
+            const int64_t lo = c * g.chunk;
+            const int n = (int)min((int64_t)g.chunk, Mb - lo);
+            const float* src = imp + t0 + lo;
+            const float x0 = lane < n ? src[lane] : 0.f;
+            const float x1 = lane + 32 < n ? src[lane + 32] : 0.f;
+            const double sum = warp_chunk_sum(x0, x1, n);
+            const double mean = n == g.chunk ? div_count(sum, n, g.rcp_chunk) : __ddiv_rn(sum, (double)n);
+            if (lane == 0) {
+                win[w] = mean;
+                if (w >= r && w < r + outs) {
+                    sums[gc] = sum;
+                    means[gc] = mean;
+                }
+            }
+        }
+    } else {
+        __shared__ double xs[64 * (kPoolWarps + 1)];   // token k of the block's chunk w at k * 33 + w
+        if (gc >= 0 && gc < total) {
+            const int b = chunk_batch(g, tb, gc);
+            const int64_t c = gc - tab_cn(g, tb, b);
+            const int64_t t0 = tab_cu(g, tb, b), Mb = tab_cu(g, tb, b + 1) - t0;
+            const int64_t lo = c * g.chunk;
+            const int n = (int)min((int64_t)g.chunk, Mb - lo);
+            const NormCoef mmb = g.normalize ? mm[b] : NormCoef{0.0, 0.0, 0.0, 1};
+            if (lane < n) xs[lane * (kPoolWarps + 1) + w] = token_score(g, imp[t0 + lo + lane], lo + lane, Mb, mmb);
+            if (lane + 32 < n)
+                xs[(lane + 32) * (kPoolWarps + 1) + w] = token_score(g, imp[t0 + lo + lane + 32], lo + lane + 32, Mb, mmb);
+        }
+        __syncthreads();
+        if (w == 0) {
+            const int64_t gcl = gc0 - r + lane;            // lane c chains the block's chunk c
+            if (gcl >= 0 && gcl < total) {
+                const int b = chunk_batch(g, tb, gcl);
+                const int64_t c = gcl - tab_cn(g, tb, b);
+                const int64_t Mb = tab_cu(g, tb, b + 1) - tab_cu(g, tb, b);
+                const int n = (int)min((int64_t)g.chunk, Mb - c * g.chunk);
+                double sum = 0.0;
+                for (int k = 0; k < n; ++k) sum = __dadd_rn(sum, xs[k * (kPoolWarps + 1) + lane]);
+                const double mean = n == g.chunk ? div_count(sum, n, g.rcp_chunk) : __ddiv_rn(sum, (double)n);
+                win[lane] = mean;
+                if (lane >= r && lane < r + outs) {
+                    sums[gcl] = sum;
+                    means[gcl] = mean;
+                }
             }
         }
     }
@@ -1114,13 +1154,14 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
         int32_t* hdr = normalize ? nullptr : static_cast<int32_t*>(ws);
         const bool pool = p.mode == SP_SELECT_TOPK && p.pool_k > 1;
         const int r = pool ? (p.pool_k - 1) / 2 : 0;
-        if (!p.has_boost && p.chunk <= 64 && r <= kMaxWarpPoolHalo) {
-            // plain scores in chunks of up to 64 tokens: a warp per chunk
+        if (p.chunk <= 64 && r <= kMaxWarpPoolHalo) {
+            // chunks of up to 64 tokens: a warp per chunk
             SelGeo gw = g;
             if (!pool) gw.pool_k = 1;
             const int outs = kPoolWarps - 2 * r;
-            SP_CUDA_TRY(launch_early(chunk_pool_warp_kernel, (unsigned)((total + outs - 1) / outs), kPoolWarps * 32, 0,
-                                     st, gw, p.importance, sums, means, pooled, hdr));
+            auto* kern = p.has_boost ? chunk_pool_warp_kernel<true> : chunk_pool_warp_kernel<false>;
+            SP_CUDA_TRY(launch_early(kern, (unsigned)((total + outs - 1) / outs), kPoolWarps * 32, 0, st, gw,
+                                     p.importance, (const NormCoef*)mm, sums, means, pooled, hdr));
             SP_LAUNCH_CHECK();
         } else if (pool && (p.pool_k - 1) / 2 <= kMaxPoolHalo) {
             const int threads = (kPoolBlock + (p.pool_k - 1) + 31) / 32 * 32;     // 64 + 2r means, whole warps
