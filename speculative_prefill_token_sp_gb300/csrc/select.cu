@@ -135,8 +135,9 @@ struct NormCoef {
 __global__ void __launch_bounds__(1024) minmax_kernel(const SelGeo g, const float* __restrict__ imp,
                                                       NormCoef* __restrict__ mm, int32_t* __restrict__ hdr) {
     const int b = blockIdx.x;
-    if (hdr != nullptr && b == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
     const int64_t m0 = geo_cu(g, b), Mb = geo_cu(g, b + 1) - m0;
+    wait_prior_grid();
+    if (hdr != nullptr && b == 0 && threadIdx.x < (int)(sizeof(WsHeader) / 4)) hdr[threadIdx.x] = 0;
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll 8
     for (int64_t i = threadIdx.x; i < Mb; i += blockDim.x) {
@@ -1146,7 +1147,8 @@ sp_status select_launch(const SelectProblem& p, void* ws, cudaStream_t st) {
     const bool normalize = p.has_boost && p.boost.normalize;
     if (total == 0) SP_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
     if (normalize && total > 0) {
-        minmax_kernel<<<p.B, 1024, 0, st>>>(g, p.importance, mm, static_cast<int32_t*>(ws));
+        SP_CUDA_TRY(launch_early(minmax_kernel, (unsigned)p.B, 1024, 0, st, g, p.importance, mm,
+                                 static_cast<int32_t*>(ws)));
         SP_LAUNCH_CHECK();
     }
     if (total > 0) {
