@@ -923,17 +923,30 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelGeo g, con
         __syncthreads();
     }
     const int kstar = s_kstar;
-    for (int k = tid; k < nc; k += nt) flags[c0 + idx[k]] = k < kstar ? 1 : 0;
+    // the kept flags also in shared memory (over the ranked prefixes, no longer needed)
+    int* kept_sh = reinterpret_cast<int*>(keys);
+    for (int k = tid; k < nc; k += nt) {
+        const int c = idx[k], f = k < kstar ? 1 : 0;
+        kept_sh[c] = f;
+        flags[c0 + c] = f;
+    }
     __syncthreads();
+    const bool narrow = Mb < (int64_t)INT32_MAX;
     long long running = 0;
     for (int base = 0; base < nc; base += nt) {
         const int c = base + tid;
         const bool in = c < nc;
-        const bool keep = in && flags[c0 + c] != 0;
+        const bool keep = in && kept_sh[c] != 0;
         const int64_t lo = (int64_t)c * g.chunk;
         const long long sz = keep ? (long long)(min(lo + (int64_t)g.chunk, Mb) - lo) : 0;
-        long long tot_sz;
-        const long long off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        long long off, tot_sz;
+        if (narrow) {
+            int t32;
+            off = block_exclusive_scan32((int)sz, scan32, &t32);
+            tot_sz = t32;
+        } else {
+            off = block_exclusive_scan(sz, scan_sh, &tot_sz);
+        }
         if (in) offs[c0 + c] = running + off;
         if (g.chunk <= kInlinePosChunk) {
             unsigned kb = __ballot_sync(0xffffffffu, keep);
