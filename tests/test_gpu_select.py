@@ -299,3 +299,21 @@ def test_mass_cut_bit_exact(sp, case):
     kind, M, chunk, tau, boost = case
     imp = _mass_inputs(kind, M, seed=M + chunk)
     assert_same(sp, imp, chunk, 1, "mass", tau, boost)
+
+
+def test_many_prompts_varlen_bit_exact(sp):
+    """A batch of 200 prompts (some empty): the selection kernels look prompts
+    up in offset tables staged in shared memory; both modes against the oracle."""
+    import torch
+    rng = np.random.default_rng(11)
+    lens = rng.integers(0, 3000, 200)
+    lens[::17] = 0
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    imp = (rng.random(int(cu[-1])) * 1e-3).astype(np.float32)
+    for chunk, mode, rate, pool, boost in ((32, "topk", 0.2, 3, None), (16, "topk", 0.3, 5, W.V3_BOOST),
+                                           (32, "mass", 0.85, 1, W.V3_BOOST), (64, "mass", 0.6, 1, None)):
+        got = sp.select_varlen(torch.from_numpy(imp).cuda(), cu, chunk, pool, mode, rate, boost)
+        torch.cuda.synchronize()
+        want = oracle.select_varlen(imp, cu, chunk, pool, mode, rate, boost)
+        for b in range(len(lens)):
+            assert np.array_equal(got[b].cpu().numpy(), want[b][0]), (mode, chunk, b)
