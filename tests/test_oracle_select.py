@@ -139,3 +139,18 @@ def test_varlen_is_per_request():
         p2, n2 = oracle.select(imp[cu[b]:cu[b + 1]], 16, 3, "topk", 0.3)
         assert n == n2 and np.array_equal(pos, p2)
         assert pos.size == 0 or pos.max() < lens[b]
+
+
+def test_varlen_hand_case():
+    """Two requests packed back to back, worked by hand (the guide's per-request
+    selection; positions are each request's own, from 0).  Request 0: scores
+    [0.9, 0.1, 0.1, 0.8], chunk 1, no pool, keep 0.5 -> kc = ceil(4 * 0.5) = 2:
+    chunks 0 and 3.  Request 1: [0.2, 0.7] -> kc = 1: chunk 1.  Mass mode,
+    tau = 0.5: request 0's total 1.9, ranked 0.9 (0.9 < 0.95), then 0.8 (1.7):
+    chunks 0 and 3; request 1's total 0.9, ranked 0.7 >= 0.45: chunk 1."""
+    imp = np.array([0.9, 0.1, 0.1, 0.8, 0.2, 0.7], dtype=np.float32)
+    cu = [0, 4, 6]
+    res = oracle.select_varlen(imp, cu, 1, 1, "topk", 0.5)
+    assert [list(p) for p, _ in res] == [[0, 3], [1]] and [n for _, n in res] == [2, 1]
+    res = oracle.select_varlen(imp, cu, 1, 1, "mass", 0.5)
+    assert [list(p) for p, _ in res] == [[0, 3], [1]]
