@@ -365,6 +365,17 @@ uint64_t sp_kernel_launches(void);
  * wide, not synchronised with calls running on other threads. */
 uint64_t sp_test_set_exchange_wait_ns(uint64_t ns);
 
+/* Test hook (host only, no device work): the tensor-core scoring path's plan
+ * for one bf16 prompt of M tokens (L layers, H query heads, H_kv KV heads, head
+ * dim d, N look-ahead steps; the first pass when N needs several) on `sms` SMs.
+ * Writes nine ints to out9 (caller-owned host memory): slab classes F, CTAs per
+ * class Pc, CTAs P = F * Pc, tiles of 128 tokens per CTA per slab, tiles per
+ * epilogue group, landing tiles per group, held slabs per group, the
+ * statistics-to-normalise lag in slabs, and the shared memory per CTA in bytes.
+ * Returns 1, or 0 when that path does not take the shape (or an argument is
+ * out of range); nothing is launched and nothing else is written. */
+int sp_test_score_plan(int L, int H, int H_kv, int d, int64_t M, int N, int sms, int* out9);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ __all__ = [
     "sp_select_workspace_size", "sp_select", "sp_select_varlen_workspace_size", "sp_select_varlen",
     "sp_select_noalloc", "sp_select_rules_workspace_size", "sp_select_rules", "SpKeepRules", "GUIDE_RULES",
     "sp_gather_kept", "sp_workspace_status", "sp_last_error", "sp_status_string", "sp_version",
-    "sp_kernel_launches", "sp_test_set_exchange_wait_ns",
+    "sp_kernel_launches", "sp_test_set_exchange_wait_ns", "sp_test_score_plan",
     "score", "score_lse", "score_prefill", "score_varlen", "score_lse_varlen", "select", "select_rules", "select_varlen", "gather_kept", "V3_BOOST",
 ]
 
@@ -92,6 +92,7 @@ _SIGS = {
     "sp_version": (_i32, []),
     "sp_kernel_launches": (_c.c_uint64, []),
     "sp_test_set_exchange_wait_ns": (_c.c_uint64, [_c.c_uint64]),
+    "sp_test_score_plan": (_i32, [_i32, _i32, _i32, _i32, _c.c_int64, _i32, _i32, _c.POINTER(_c.c_int)]),
 }
 
 
@@ -284,6 +285,17 @@ def sp_test_set_exchange_wait_ns(ns: int) -> int:
     """Test hook: limit (ns) of the scoring kernel's waits on other CTAs' exchange
     entries; 0 restores the default.  Returns the previous limit."""
     return lib().sp_test_set_exchange_wait_ns(int(ns))
+
+
+def sp_test_score_plan(L: int, H: int, H_kv: int, d: int, M: int, N: int, sms: int = 152):
+    """Test hook: the tensor-core scoring plan of one bf16 prompt as a dict
+    (F, Pc, P, tiles, tiles_per_group, land, held, lag, smem_bytes), or None when
+    that path does not take the shape.  Host only."""
+    out = (_c.c_int * 9)()
+    if not lib().sp_test_score_plan(L, H, H_kv, d, int(M), N, sms, out):
+        return None
+    keys = ("F", "Pc", "P", "tiles", "tiles_per_group", "land", "held", "lag", "smem_bytes")
+    return dict(zip(keys, list(out)))
 
 
 # ----------------------------------------------------------------------------

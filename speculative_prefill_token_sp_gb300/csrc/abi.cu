@@ -43,6 +43,7 @@ bool score_tc_supported(const ScoreProblem& p);
 size_t score_tc_ws_bytes(const ScoreProblem& p);
 sp_status score_tc_launch(const ScoreProblem& p, void* ws, cudaStream_t st);
 unsigned long long score_tc_set_exchange_wait_ns(unsigned long long ns);
+bool score_tc_plan_of(int L, int H, int H_kv, int d, int64_t M, int N, int sms, int out[9]);
 
 }  // namespace sp
 
@@ -514,5 +515,10 @@ int sp_version(void) { return 100; }
 uint64_t sp_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 uint64_t sp_test_set_exchange_wait_ns(uint64_t ns) { return score_tc_set_exchange_wait_ns(ns); }
+
+int sp_test_score_plan(int L, int H, int H_kv, int d, int64_t M, int N, int sms, int* out9) {
+    if (out9 == nullptr || sms < 1 || M < 1 || N < 1) return 0;
+    return score_tc_plan_of(L, H, H_kv, d, M, N, sms, out9) ? 1 : 0;
+}
 
 }  // extern "C"

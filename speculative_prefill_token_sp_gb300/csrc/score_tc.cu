@@ -1627,8 +1627,25 @@ unsigned long long score_tc_set_exchange_wait_ns(unsigned long long ns) {
     return g_exchange_wait_ns.exchange(ns == 0 ? kTimeoutNs : ns);
 }
 
+
 // The first pass has the most steps (the largest workspace).
 Pass first_pass(const ScoreProblem& q) { return Pass{0, std::min(q.N, steps_per_pass(q))}; }
+
+// The plan of one bf16 prompt of M tokens on `sms` SMs (first pass), for tests
+// of the planner: out = {F, Pc, P, n_tiles_max, tiles_per_group, land, held,
+// lag, smem_bytes}.  Returns false when the tensor-core path does not take it.
+bool score_tc_plan_of(int L, int H, int H_kv, int d, int64_t M, int N, int sms, int out[9]) {
+    ScoreProblem q{};
+    q.B = 1; q.L = L; q.H = H; q.H_kv = H_kv; q.d = d; q.N = N;
+    q.T = M; q.max_M = M; q.dtype = SP_BF16;
+    if (H_kv < 1 || H % H_kv != 0 || !shape_ok(q)) return false;
+    Plan plan;
+    if (!make_plan(q, M, sms, first_pass(q), plan)) return false;
+    const TcParams& p = plan.p;
+    const int v[9] = {p.F, p.Pc, p.P, p.n_tiles_max, p.tiles_per_group, p.land, p.held, p.lag, p.smem_bytes};
+    for (int i = 0; i < 9; ++i) out[i] = v[i];
+    return true;
+}
 
 bool score_tc_supported(const ScoreProblem& q) {
     Plan plan;
